@@ -1,0 +1,30 @@
+"""CPU oracle for the AWQ W4A16 linear forward -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The library under
+``bit_weight_quantized_awq_gb300`` never does, and shares no code with it.
+
+Pinned functions (each one is checked by ``tests/test_oracle_pins.py``
+against something other than itself):
+
+* ``f64_to_f16_bits`` / ``f16_bits_to_f64`` -- IEEE binary16 written from its
+  definition; pinned against numpy's correctly rounded conversion on every
+  bit pattern and on every halfway case.
+* ``unpack`` -- nibble i of int32 j holds column 8j + i; pinned by hand-packed
+  hex fixtures in ``tests/golden/`` and by a one-hot placement test.
+* ``dequant`` -- fp16_rn((q - z) * scale) per group of ``group_size`` input
+  rows; pinned by exhaustive (q, z) x scale sweeps against exact rational
+  arithmetic and by hand cases.
+* ``forward`` -- fp64 sum over k of x * W16, plus bias; pinned by integer brute
+  force on hand cases, the q == z identity, g = -1 vs g = K, scale doubling,
+  per-group additivity and a library (numpy fp64 matmul) cross-check.
+"""
+from .oracle import (  # noqa: F401
+    build,
+    f64_to_f16_bits,
+    f16_bits_to_f64,
+    resolve_group,
+    unpack,
+    dequant,
+    forward,
+)
