@@ -1,1 +1,26 @@
-"""GB300 (sm_103a) AWQ W4A16 linear forward (placeholder while the binding is written)."""
+"""GB300 (sm_103a) AWQ W4A16 linear forward.
+
+``y = x . dequant(W) + bias`` with W held as 4-bit codes packed eight per
+int32 (nibble i of int32 j holds column 8j + i), per-group packed zero points
+and fp16 scales -- the WQLinear layer of the Predibase Lorax "AWQ WQLinear"
+page. The computation runs in hand-written CUDA kernels behind the C ABI in
+``include/awq_gb300.h``; this package is the binding (``_binding``), a torch
+wrapper (``layer``) and a seeded input generator (``synthetic``).
+"""
+from ._binding import (  # noqa: F401
+    EXPORTED,
+    LIB_PATH,
+    AWQError,
+    Path,
+    Status,
+    awq_dequant,
+    awq_last_device_status,
+    awq_linear_forward,
+    awq_linear_forward_path,
+    awq_path_supported,
+    awq_select_path,
+    awq_shutdown,
+    awq_status_string,
+    load_library,
+)
+from .layer import AWQLinear, dequant, linear_forward  # noqa: F401

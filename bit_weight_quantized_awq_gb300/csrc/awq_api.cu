@@ -1,0 +1,277 @@
+// awq_api.cu -- the C ABI (include/awq_gb300.h): argument checks, path
+// choice, per-(device, stream) scratch and the device status word.
+//
+// The argument checks are the WQLinear page's construction rules (Predibase
+// Lorax "AWQ WQLinear", Description, __init__ bullets): w_bit is 4 (implicit:
+// the ABI has no other width), out_features = 8 x qweight columns so
+// N % 8 == 0, group_size -1 means K, and K % group_size == 0. Where the page
+// asserts, this layer returns a status instead; nothing aborts.
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/awq_gb300.h"
+#include "awq_internal.h"
+
+namespace awq {
+
+// ---------------------------------------------------------------------------
+// device status word: one per device that loads the library
+// ---------------------------------------------------------------------------
+
+__device__ unsigned int g_device_status = 0;
+
+namespace {
+
+std::mutex g_mutex;
+std::map<int, unsigned int *> g_status_addr;                  // device -> &g_device_status
+
+struct ScratchEntry {
+    float *partials = nullptr;
+    size_t partial_floats = 0;
+    unsigned int *counters = nullptr;
+    size_t n_counters = 0;
+};
+std::map<std::pair<int, cudaStream_t>, ScratchEntry> g_scratch;
+
+} // namespace
+
+unsigned int *device_status_word()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    auto it = g_status_addr.find(dev);
+    if (it != g_status_addr.end()) return it->second;
+    void *addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return nullptr;
+    g_status_addr[dev] = static_cast<unsigned int *>(addr);
+    return static_cast<unsigned int *>(addr);
+}
+
+bool get_scratch(cudaStream_t stream, size_t partial_floats, size_t n_counters, Scratch *out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    ScratchEntry &e = g_scratch[std::make_pair(dev, stream)];
+    if (e.partial_floats < partial_floats) {
+        // the old area may still be read by work queued on this stream
+        if (e.partials) {
+            cudaStreamSynchronize(stream);
+            cudaFree(e.partials);
+            e.partials = nullptr;
+            e.partial_floats = 0;
+        }
+        size_t want = partial_floats + partial_floats / 2;
+        if (cudaMalloc(&e.partials, want * sizeof(float)) != cudaSuccess) {
+            e.partials = nullptr;
+            return false;
+        }
+        e.partial_floats = want;
+    }
+    if (e.n_counters < n_counters) {
+        if (e.counters) {
+            cudaStreamSynchronize(stream);
+            cudaFree(e.counters);
+            e.counters = nullptr;
+            e.n_counters = 0;
+        }
+        size_t want = n_counters + n_counters / 2 + 64;
+        if (cudaMalloc(&e.counters, want * sizeof(unsigned int)) != cudaSuccess) {
+            e.counters = nullptr;
+            return false;
+        }
+        // counters start at zero; every kernel leaves them at zero again
+        if (cudaMemsetAsync(e.counters, 0, want * sizeof(unsigned int), stream) != cudaSuccess)
+            return false;
+        e.n_counters = want;
+    }
+    out->partials = e.partials;
+    out->partial_floats = e.partial_floats;
+    out->counters = e.counters;
+    out->n_counters = e.n_counters;
+    return true;
+}
+
+// Drops the counters of every scratch area on this device so that the next
+// call re-zeroes them (used after a device-side timeout left some non-zero).
+static void reset_scratch_counters(int dev)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    for (auto &kv : g_scratch) {
+        if (kv.first.first != dev) continue;
+        if (kv.second.counters) cudaFree(kv.second.counters);
+        kv.second.counters = nullptr;
+        kv.second.n_counters = 0;
+    }
+}
+
+} // namespace awq
+
+using awq::Problem;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The WQLinear page's shape rules; fills the resolved group size.
+awq_status_t check_shape(int64_t K, int64_t N, int64_t group_size, int64_t *g_out)
+{
+    if (K <= 0 || N <= 0) return AWQ_ERR_INVALID_ARG;
+    if (N % 8 != 0) return AWQ_ERR_INVALID_ARG;
+    if (group_size == 0 || group_size < -1) return AWQ_ERR_INVALID_ARG;
+    const int64_t g = (group_size == -1) ? K : group_size;
+    if (K % g != 0) return AWQ_ERR_INVALID_ARG;
+    *g_out = g;
+    return AWQ_OK;
+}
+
+bool path_fits(const Problem &p, awq_path_t path)
+{
+    switch (path) {
+    case AWQ_PATH_GENERIC: return true;
+    case AWQ_PATH_DECODE: return awq::decode_supported(p.M, p.K, p.N, p.g);
+    case AWQ_PATH_PREFILL: return awq::prefill_supported(p.M, p.K, p.N, p.g);
+    default: return false;
+    }
+}
+
+// Largest M served by the decode kernel when both fast paths fit.
+constexpr int64_t kDecodeMaxM = 16;
+
+awq_path_t auto_path(const Problem &p)
+{
+    if (p.M <= kDecodeMaxM && awq::decode_supported(p.M, p.K, p.N, p.g)) return AWQ_PATH_DECODE;
+    if (awq::prefill_supported(p.M, p.K, p.N, p.g)) return AWQ_PATH_PREFILL;
+    if (awq::decode_supported(p.M, p.K, p.N, p.g)) return AWQ_PATH_DECODE;
+    return AWQ_PATH_GENERIC;
+}
+
+} // namespace
+
+extern "C" {
+
+const char *awq_status_string(awq_status_t status)
+{
+    switch (status) {
+    case AWQ_OK: return "AWQ_OK";
+    case AWQ_ERR_INVALID_ARG: return "AWQ_ERR_INVALID_ARG: shape rule violated, NULL pointer or M < 0";
+    case AWQ_ERR_MISALIGNED: return "AWQ_ERR_MISALIGNED: a base pointer is not 16-byte aligned";
+    case AWQ_ERR_CUDA: return "AWQ_ERR_CUDA: a CUDA call or kernel launch failed";
+    case AWQ_ERR_TIMEOUT: return "AWQ_ERR_TIMEOUT: a kernel's bounded wait ran out";
+    default: return "AWQ: unknown status";
+    }
+}
+
+int awq_path_supported(int64_t M, int64_t K, int64_t N, int64_t group_size, awq_path_t path)
+{
+    int64_t g = 0;
+    if (M < 0 || check_shape(K, N, group_size, &g) != AWQ_OK) return 0;
+    Problem p{};
+    p.M = M; p.K = K; p.N = N; p.g = g; p.G = K / g;
+    return path_fits(p, path) ? 1 : 0;
+}
+
+int awq_select_path(int64_t M, int64_t K, int64_t N, int64_t group_size)
+{
+    int64_t g = 0;
+    if (M < 0 || check_shape(K, N, group_size, &g) != AWQ_OK) return -1;
+    Problem p{};
+    p.M = M; p.K = K; p.N = N; p.g = g; p.G = K / g;
+    return (int)auto_path(p);
+}
+
+awq_status_t awq_linear_forward_path(const void *x, const int32_t *qweight, const int32_t *qzeros,
+                                     const void *scales, const void *bias, void *y, int64_t M,
+                                     int64_t K, int64_t N, int64_t group_size, awq_stream_t stream,
+                                     awq_path_t path)
+{
+    int64_t g = 0;
+    if (M < 0) return AWQ_ERR_INVALID_ARG;
+    awq_status_t st = check_shape(K, N, group_size, &g);
+    if (st != AWQ_OK) return st;
+    if (!x || !qweight || !qzeros || !scales || !y) return AWQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(qweight) || !aligned16(qzeros) || !aligned16(scales) ||
+        !aligned16(y) || (bias && !aligned16(bias)))
+        return AWQ_ERR_MISALIGNED;
+    if (path != AWQ_PATH_AUTO && path != AWQ_PATH_GENERIC && path != AWQ_PATH_DECODE &&
+        path != AWQ_PATH_PREFILL)
+        return AWQ_ERR_INVALID_ARG;
+    Problem p{x, qweight, qzeros, scales, bias, y, M, K, N, g, K / g};
+    if (path != AWQ_PATH_AUTO && !path_fits(p, path)) return AWQ_ERR_INVALID_ARG;
+    if (M == 0) return AWQ_OK;
+    const awq_path_t use = (path == AWQ_PATH_AUTO) ? auto_path(p) : path;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (use) {
+    case AWQ_PATH_DECODE: e = awq::launch_decode(p, s); break;
+    case AWQ_PATH_PREFILL: e = awq::launch_prefill(p, s); break;
+    default: e = awq::launch_generic(p, s); break;
+    }
+    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+}
+
+awq_status_t awq_linear_forward(const void *x, const int32_t *qweight, const int32_t *qzeros,
+                                const void *scales, const void *bias, void *y, int64_t M,
+                                int64_t K, int64_t N, int64_t group_size, awq_stream_t stream)
+{
+    return awq_linear_forward_path(x, qweight, qzeros, scales, bias, y, M, K, N, group_size,
+                                   stream, AWQ_PATH_AUTO);
+}
+
+awq_status_t awq_dequant(const int32_t *qweight, const int32_t *qzeros, const void *scales,
+                         void *W, int64_t K, int64_t N, int64_t group_size, awq_stream_t stream)
+{
+    int64_t g = 0;
+    awq_status_t st = check_shape(K, N, group_size, &g);
+    if (st != AWQ_OK) return st;
+    if (!qweight || !qzeros || !scales || !W) return AWQ_ERR_INVALID_ARG;
+    if (!aligned16(qweight) || !aligned16(qzeros) || !aligned16(scales) || !aligned16(W))
+        return AWQ_ERR_MISALIGNED;
+    Problem p{nullptr, qweight, qzeros, scales, nullptr, nullptr, 0, K, N, g, K / g};
+    cudaError_t e = awq::launch_dequant(p, W, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+}
+
+awq_status_t awq_last_device_status(awq_stream_t stream)
+{
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return AWQ_ERR_CUDA;
+    unsigned int *addr = awq::device_status_word();
+    if (!addr) return AWQ_ERR_CUDA;
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, addr, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return AWQ_ERR_CUDA;
+    if (word == 0) return AWQ_OK;
+    const unsigned int zero = 0;
+    if (cudaMemcpy(addr, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+        return AWQ_ERR_CUDA;
+    if (word & awq::kStatusTimeout) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        awq::reset_scratch_counters(dev);
+        return AWQ_ERR_TIMEOUT;
+    }
+    return AWQ_ERR_CUDA;
+}
+
+void awq_shutdown(void)
+{
+    std::lock_guard<std::mutex> lock(awq::g_mutex);
+    int prev = 0;
+    cudaGetDevice(&prev);
+    for (auto &kv : awq::g_scratch) {
+        cudaSetDevice(kv.first.first);
+        if (kv.second.partials) cudaFree(kv.second.partials);
+        if (kv.second.counters) cudaFree(kv.second.counters);
+    }
+    awq::g_scratch.clear();
+    cudaSetDevice(prev);
+}
+
+} // extern "C"

@@ -1,0 +1,59 @@
+// awq_dequant.cu -- the awq_dequant kernel: packed int4 weights -> fp16 W.
+//
+// Predibase Lorax "AWQ WQLinear" page, Description (__init__: per-group
+// dequantisation; qweight packs eight 4-bit values per int32):
+//   W[k, n] = fp16_rn((q[k, n] - z[k / g, n]) * scales[k / g, n]).
+//
+// HBM-bound elementwise work: per packed int32 read (4 B) it writes 8 fp16
+// (16 B); scales and zero points are re-read by the g rows of a group and stay
+// in L2. One thread handles one packed word: a coalesced 4-byte load and one
+// 16-byte store per thread. The grid is a multiple of the SM count and
+// strides over the K x N/8 words.
+#include "awq_device.cuh"
+#include "awq_internal.h"
+
+namespace awq {
+namespace {
+
+__global__ void __launch_bounds__(256)
+dequant_kernel(const uint32_t *__restrict__ qweight, const uint32_t *__restrict__ qzeros,
+               const __half *__restrict__ scales, __half *__restrict__ W,
+               int64_t K, int64_t words, int64_t g)
+{
+    const int64_t total = K * words;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t k = idx / words;
+        const int64_t j = idx - k * words;
+        const int64_t gi = k / g;
+        const uint32_t qw = __ldg(qweight + idx);
+        const uint32_t zw = __ldg(qzeros + gi * words + j);
+        // 8 scales of columns 8j .. 8j+7: 16 bytes, 16-byte aligned
+        const uint4 sraw = __ldg(reinterpret_cast<const uint4 *>(scales + (gi * words + j) * 8));
+        __half s[8], w[8];
+        *reinterpret_cast<uint4 *>(s) = sraw;
+        dequant_word(qw, zw, s, w);
+        *reinterpret_cast<uint4 *>(W + idx * 8) = *reinterpret_cast<const uint4 *>(w);
+    }
+}
+
+} // namespace
+
+cudaError_t launch_dequant(const Problem &p, void *W, cudaStream_t stream)
+{
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t words = p.N / 8;
+    const int64_t total = p.K * words;
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    const int64_t cap = (int64_t)(sms > 0 ? sms : 1) * 8;
+    if (blocks > cap) blocks = cap;
+    dequant_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
+        reinterpret_cast<const uint32_t *>(p.qweight), reinterpret_cast<const uint32_t *>(p.qzeros),
+        static_cast<const __half *>(p.scales), static_cast<__half *>(W), p.K, words, p.g);
+    return cudaGetLastError();
+}
+
+} // namespace awq

@@ -1,0 +1,55 @@
+// awq_internal.h -- host-side interface between the C-ABI layer (awq_api.cu)
+// and the kernel translation units. Not installed; not part of the ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace awq {
+
+// One validated forward/dequant problem. g is the resolved group size (the
+// page's group_size -1 already replaced by K), G = K / g.
+struct Problem {
+    const void *x;          // fp16 [M, K]
+    const int32_t *qweight; // int32 [K, N / 8]
+    const int32_t *qzeros;  // int32 [G, N / 8]
+    const void *scales;     // fp16 [G, N]
+    const void *bias;       // fp16 [N] or nullptr
+    void *y;                // fp16 [M, N]
+    int64_t M, K, N, g, G;
+};
+
+// Per-(device, stream) scratch: fp32 split-K partials plus self-resetting
+// per-tile arrival counters (zero between calls).
+struct Scratch {
+    float *partials;
+    size_t partial_floats;
+    unsigned int *counters;
+    size_t n_counters;
+};
+
+// Returns the address of this device's status word (bit flags, see
+// kStatusTimeout) for kernels to record device-side errors in.
+unsigned int *device_status_word();
+constexpr unsigned int kStatusTimeout = 1u;
+
+// Scratch for `stream` on the current device, grown to at least the given
+// sizes. Returns false if an allocation failed.
+bool get_scratch(cudaStream_t stream, size_t partial_floats, size_t n_counters, Scratch *out);
+
+// ---- kernel launchers (each returns the launch's cudaError_t) ----
+
+cudaError_t launch_dequant(const Problem &p, void *W, cudaStream_t stream);
+
+cudaError_t launch_generic(const Problem &p, cudaStream_t stream);
+
+// Decode path (small M). supported_* is host-only shape logic.
+bool decode_supported(int64_t M, int64_t K, int64_t N, int64_t g);
+cudaError_t launch_decode(const Problem &p, cudaStream_t stream);
+
+// Prefill path (large M, tcgen05).
+bool prefill_supported(int64_t M, int64_t K, int64_t N, int64_t g);
+cudaError_t launch_prefill(const Problem &p, cudaStream_t stream);
+
+} // namespace awq

@@ -1,0 +1,121 @@
+"""Torch-facing wrappers: allocate outputs, pass pointers and the current
+stream to the C ABI, reshape. No arithmetic happens here.
+
+``AWQLinear`` follows the WQLinear contract (Predibase Lorax "AWQ WQLinear"
+page): constructor arguments (w_bit, group_size, qweight, qzeros, scales,
+bias) from its Signature; the w_bit == 4, shape and divisibility checks from
+Description, __init__; forward = flatten x to 2-D, quantised GEMM, bias,
+restore the batch shape (Description, forward steps 1-3); a ``weight``
+property returning the raw qweight.
+"""
+from __future__ import annotations
+
+import torch
+
+from ._binding import AWQError, Path, Status, awq_dequant, awq_linear_forward_path
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check(t: torch.Tensor, name: str, dtype: torch.dtype, device: torch.device):
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def linear_forward(x: torch.Tensor, qweight: torch.Tensor, qzeros: torch.Tensor,
+                   scales: torch.Tensor, bias: torch.Tensor | None, group_size: int,
+                   path: Path = Path.AUTO, out: torch.Tensor | None = None) -> torch.Tensor:
+    """y = x . dequant(qweight, qzeros, scales) + bias, shape (*x.shape[:-1], N)."""
+    dev = qweight.device
+    if dev.type != "cuda":
+        raise ValueError("the AWQ library runs on CUDA tensors only")
+    _check(x, "x", torch.float16, dev)
+    _check(qweight, "qweight", torch.int32, dev)
+    _check(qzeros, "qzeros", torch.int32, dev)
+    _check(scales, "scales", torch.float16, dev)
+    if bias is not None:
+        _check(bias, "bias", torch.float16, dev)
+    K, N = qweight.shape[0], qweight.shape[1] * 8
+    if x.shape[-1] != K:
+        raise ValueError(f"x has {x.shape[-1]} input features, qweight has {K}")
+    M = x.numel() // K
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=dev)
+    else:
+        _check(out, "out", torch.float16, dev)
+        if out.numel() != M * N:
+            raise ValueError("out has the wrong number of elements")
+    st = awq_linear_forward_path(_ptr(x), _ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(bias),
+                                 _ptr(out), M, K, N, group_size, _stream(dev), int(path))
+    if st != Status.OK:
+        raise AWQError(st, "awq_linear_forward")
+    return out.view(*x.shape[:-1], N)
+
+
+def dequant(qweight: torch.Tensor, qzeros: torch.Tensor, scales: torch.Tensor,
+            group_size: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """W [K, N] fp16 = (q - z) * scale per group, rounded once to fp16."""
+    dev = qweight.device
+    if dev.type != "cuda":
+        raise ValueError("the AWQ library runs on CUDA tensors only")
+    _check(qweight, "qweight", torch.int32, dev)
+    _check(qzeros, "qzeros", torch.int32, dev)
+    _check(scales, "scales", torch.float16, dev)
+    K, N = qweight.shape[0], qweight.shape[1] * 8
+    if out is None:
+        out = torch.empty((K, N), dtype=torch.float16, device=dev)
+    else:
+        _check(out, "out", torch.float16, dev)
+    st = awq_dequant(_ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(out), K, N, group_size,
+                     _stream(dev))
+    if st != Status.OK:
+        raise AWQError(st, "awq_dequant")
+    return out
+
+
+class AWQLinear(torch.nn.Module):
+    """4-bit weight-only quantised linear layer (W4A16), inference only."""
+
+    def __init__(self, w_bit: int, group_size: int, qweight: torch.Tensor, qzeros: torch.Tensor,
+                 scales: torch.Tensor, bias: torch.Tensor | None):
+        super().__init__()
+        if w_bit != 4:
+            raise ValueError("only 4-bit weights are supported")
+        self.w_bit = w_bit
+        self.in_features = qweight.shape[0]
+        self.out_features = qweight.shape[1] * 32 // w_bit
+        self.group_size = self.in_features if group_size == -1 else group_size
+        if self.group_size <= 0 or self.in_features % self.group_size != 0:
+            raise ValueError("in_features must be divisible by group_size")
+        if self.out_features % (32 // w_bit) != 0:
+            raise ValueError("out_features must be divisible by 8")
+        G = self.in_features // self.group_size
+        if tuple(qzeros.shape) != (G, self.out_features // 8):
+            raise ValueError(f"qzeros must have shape {(G, self.out_features // 8)}")
+        if tuple(scales.shape) != (G, self.out_features):
+            raise ValueError(f"scales must have shape {(G, self.out_features)}")
+        if bias is not None and tuple(bias.shape) != (self.out_features,):
+            raise ValueError(f"bias must have shape {(self.out_features,)}")
+        self.register_buffer("qweight", qweight)
+        self.register_buffer("qzeros", qzeros)
+        self.register_buffer("scales", scales)
+        self.register_buffer("bias", bias)
+
+    @property
+    def weight(self) -> torch.Tensor:
+        return self.qweight
+
+    @torch.no_grad()
+    def forward(self, x: torch.Tensor, path: Path = Path.AUTO) -> torch.Tensor:
+        return linear_forward(x, self.qweight, self.qzeros, self.scales, self.bias,
+                              self.group_size, path=path)

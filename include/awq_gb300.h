@@ -1,0 +1,152 @@
+/*
+ * awq_gb300.h -- C ABI of the GB300 (sm_103a) AWQ W4A16 linear-forward library.
+ *
+ * The operation (Predibase Lorax "AWQ WQLinear" page):
+ *   - Overview: a 4-bit weight-quantised linear layer, GEMM with group-wise
+ *     scaling.
+ *   - I/O Contract: qweight is int32 [in_features, out_features / 8] holding
+ *     eight 4-bit values per int32; qzeros are packed zero points; scales are
+ *     per-group scale factors; bias is optional; the output has shape
+ *     (*input_shape[:-1], out_features).
+ *   - Description, __init__: only w_bit = 4; in_features = rows of qweight;
+ *     out_features = 8 x its columns; group_size -1 means one group spanning
+ *     in_features; in_features % group_size == 0 and out_features % 8 == 0.
+ *   - Description, forward: flatten x to 2-D, run the quantised GEMM with a
+ *     pack factor of 8, add the optional bias, restore the batch shape.
+ *
+ * Notation: M = rows of x (tokens), K = in_features, N = out_features,
+ * g = group_size (g = -1 is read as g = K), G = K / g.
+ *
+ *   W[k, n] = fp16_rn( (q[k, n] - z[k / g, n]) * scales[k / g, n] )
+ *   y[m, n] = fp16_rn( sum_k x[m, k] * W[k, n]  +  bias[n] )
+ *
+ * Readings this library fixes where the page is silent:
+ *   - packing: nibble i (bits 4i .. 4i+3, lowest first) of int32 j in a row
+ *     holds column 8j + i. qzeros uses the same order, shape [G, N / 8].
+ *   - scales: fp16 [G, N]; x, bias, y, W: fp16. q and z are unsigned 0..15.
+ *   - the dequantised weight is rounded once to fp16 (round to nearest even)
+ *     before it enters the product; the sum over k is accumulated in fp32;
+ *     the bias is added to the fp32 sum and the result is rounded once.
+ *
+ * Conventions for every call below:
+ *   - All tensors are device pointers to row-major, contiguous arrays, and
+ *     every base pointer must be 16-byte aligned (AWQ_ERR_MISALIGNED if not).
+ *   - The caller owns every buffer; outputs are caller-allocated.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *     Argument errors are returned before anything is enqueued. A device-side
+ *     error (a bounded wait that timed out) is recorded in a per-device status
+ *     word that awq_last_device_status() reads.
+ *   - The library keeps, per (device, stream), a lazily created scratch area
+ *     for split-K partial sums (allocated with cudaMalloc on first use on that
+ *     stream, freed by awq_shutdown). Make the first call on a stream before
+ *     capturing that stream into a CUDA graph.
+ *   - Thread safety: calls may come from several host threads; calls on the
+ *     same stream are ordered by the stream.
+ */
+#ifndef AWQ_GB300_H
+#define AWQ_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; declared here so that this header
+ * needs no CUDA header. */
+typedef struct CUstream_st *awq_stream_t;
+
+typedef enum {
+    AWQ_OK = 0,
+    AWQ_ERR_INVALID_ARG = 1, /* a shape rule of the WQLinear page, a NULL required pointer, M < 0 */
+    AWQ_ERR_MISALIGNED = 2,  /* a base pointer is not 16-byte aligned */
+    AWQ_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed */
+    AWQ_ERR_TIMEOUT = 4      /* a kernel's bounded wait ran out (device status only) */
+} awq_status_t;
+
+/* Which kernel family serves a forward call. */
+typedef enum {
+    AWQ_PATH_AUTO = 0,    /* pick by shape (M against the measured crossover) */
+    AWQ_PATH_GENERIC = 1, /* any valid shape; plain CUDA-core kernel */
+    AWQ_PATH_DECODE = 2,  /* small M: split-K streaming GEMV-style kernel */
+    AWQ_PATH_PREFILL = 3  /* large M: tcgen05 / TMEM tensor-core kernel */
+} awq_path_t;
+
+/*
+ * awq_linear_forward -- the WQLinear forward (Description, forward steps 2-3):
+ *   y[M, N] = fp16_rn(x[M, K] . W[K, N] + bias[N]), W dequantised per group.
+ *
+ *   x          fp16 [M, K]                      (read)
+ *   qweight    int32 [K, N / 8]                 (read)
+ *   qzeros     int32 [G, N / 8]                 (read)
+ *   scales     fp16 [G, N]                      (read)
+ *   bias       fp16 [N], or NULL for no bias    (read)
+ *   y          fp16 [M, N]                      (written; must not alias inputs)
+ *   M          rows of x; M == 0 returns AWQ_OK and enqueues nothing
+ *   K, N       in_features, out_features (N % 8 == 0)
+ *   group_size g > 0 with K % g == 0, or -1 for g = K
+ *   stream     CUDA stream to enqueue on
+ *
+ * Returns AWQ_ERR_INVALID_ARG for N % 8 != 0, K % g != 0, g == 0, g < -1,
+ * M < 0, K <= 0, N <= 0 or a NULL required pointer; AWQ_ERR_MISALIGNED for a
+ * pointer that is not 16-byte aligned; AWQ_ERR_CUDA if a launch failed.
+ */
+awq_status_t awq_linear_forward(const void *x, const int32_t *qweight,
+                                const int32_t *qzeros, const void *scales,
+                                const void *bias, void *y, int64_t M, int64_t K,
+                                int64_t N, int64_t group_size, awq_stream_t stream);
+
+/*
+ * awq_linear_forward_path -- awq_linear_forward with the kernel family
+ * chosen by the caller (benchmarks and tests use it to time or check one
+ * path at every M). Same arguments, same result within the same tolerance.
+ * Returns AWQ_ERR_INVALID_ARG if `path` cannot serve this shape
+ * (awq_path_supported tells beforehand).
+ */
+awq_status_t awq_linear_forward_path(const void *x, const int32_t *qweight,
+                                     const int32_t *qzeros, const void *scales,
+                                     const void *bias, void *y, int64_t M, int64_t K,
+                                     int64_t N, int64_t group_size, awq_stream_t stream,
+                                     awq_path_t path);
+
+/* 1 if `path` can serve this (valid) shape, else 0. Host-only, no CUDA call. */
+int awq_path_supported(int64_t M, int64_t K, int64_t N, int64_t group_size, awq_path_t path);
+
+/* The path AWQ_PATH_AUTO picks for this shape (AWQ_PATH_GENERIC if only the
+ * generic kernel fits). Host-only, no CUDA call. Returns -1 for an invalid shape. */
+int awq_select_path(int64_t M, int64_t K, int64_t N, int64_t group_size);
+
+/*
+ * awq_dequant -- unpack and dequantise the packed weights (the per-group
+ * dequantisation of the WQLinear page, Description, __init__ bullet 3):
+ *   W[k, n] = fp16_rn((q[k, n] - z[k / g, n]) * scales[k / g, n])
+ *
+ *   qweight int32 [K, N / 8], qzeros int32 [G, N / 8], scales fp16 [G, N]  (read)
+ *   W       fp16 [K, N]                                                   (written)
+ * Same argument rules and statuses as awq_linear_forward (no M).
+ */
+awq_status_t awq_dequant(const int32_t *qweight, const int32_t *qzeros,
+                         const void *scales, void *W, int64_t K, int64_t N,
+                         int64_t group_size, awq_stream_t stream);
+
+/* Static description of a status code. Never NULL. */
+const char *awq_status_string(awq_status_t status);
+
+/*
+ * awq_last_device_status -- synchronises `stream`, then reads and clears the
+ * current device's status word. Returns AWQ_OK, AWQ_ERR_TIMEOUT if a kernel's
+ * bounded wait ran out since the last read (that kernel wrote no result and
+ * the scratch area of the stream it ran on is reset), or AWQ_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+awq_status_t awq_last_device_status(awq_stream_t stream);
+
+/* Frees every scratch area the library allocated, on every device. Call it
+ * only when no call of this library is in flight. Later calls allocate again. */
+void awq_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AWQ_GB300_H */

@@ -1,0 +1,138 @@
+"""Host-only checks of the C ABI: the library builds and loads, exports every
+function ``include/awq_gb300.h`` declares, and returns the documented status
+for every invalid argument before any CUDA call (so these run without a GPU).
+
+Shape rules: Predibase Lorax "AWQ WQLinear" page, Description, __init__
+(w_bit 4, out_features % 8 == 0, group_size -1 -> in_features,
+in_features % group_size == 0).
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+import bit_weight_quantized_awq_gb300 as awq
+from bit_weight_quantized_awq_gb300 import Path, Status
+from bit_weight_quantized_awq_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "awq_gb300.h")
+
+A = 0x10000      # 16-byte aligned fake device address: never dereferenced here
+B = 0x20000
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build(quiet=True)
+    return awq.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(awq_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert set(names) == set(awq.EXPORTED)
+    out = subprocess.run(["nm", "-D", "--defined-only", awq.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(awq_\w+)", out))
+    for n in names:
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_status_strings(lib):
+    for s in Status:
+        text = awq.awq_status_string(s)
+        assert text.startswith("AWQ_"), text
+    assert "unknown" in awq.awq_status_string(99)
+
+
+def fwd(M=4, K=256, N=64, g=128, x=A, qw=A, qz=A, sc=A, bias=None, y=B, path=Path.AUTO):
+    return awq.awq_linear_forward_path(x, qw, qz, sc, bias, y, M, K, N, g, None, path)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(N=12), dict(N=0), dict(N=-8), dict(K=0), dict(K=-1), dict(g=0), dict(g=-2),
+    dict(g=100), dict(K=256, g=512), dict(M=-1),
+    dict(x=None), dict(qw=None), dict(qz=None), dict(sc=None), dict(y=None),
+])
+def test_forward_invalid_args(lib, kw):
+    assert fwd(**kw) == Status.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(x=A + 2), dict(qw=A + 4), dict(qz=A + 8), dict(sc=A + 2),
+                                dict(y=B + 2), dict(bias=A + 6)])
+def test_forward_misaligned(lib, kw):
+    assert fwd(**kw) == Status.ERR_MISALIGNED
+
+
+def test_forward_m_zero_is_noop(lib):
+    assert fwd(M=0) == Status.OK
+    assert fwd(M=0, g=-1) == Status.OK
+    assert awq.awq_linear_forward(A, A, A, A, None, B, 0, 4096, 8, -1, None) == Status.OK
+
+
+def test_forward_bad_path(lib):
+    assert fwd(path=7) == Status.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(N=12), dict(g=0), dict(g=-3), dict(K=256, g=96)])
+def test_dequant_invalid(lib, kw):
+    K, N, g = kw.get("K", 256), kw.get("N", 64), kw.get("g", 128)
+    assert awq.awq_dequant(A, A, A, B, K, N, g, None) == Status.ERR_INVALID_ARG
+
+
+def test_dequant_null_and_misaligned(lib):
+    assert awq.awq_dequant(None, A, A, B, 256, 64, 128, None) == Status.ERR_INVALID_ARG
+    assert awq.awq_dequant(A, A, A, None, 256, 64, 128, None) == Status.ERR_INVALID_ARG
+    assert awq.awq_dequant(A + 4, A, A, B, 256, 64, 128, None) == Status.ERR_MISALIGNED
+    assert awq.awq_dequant(A, A, A, B + 8, 256, 64, 128, None) == Status.ERR_MISALIGNED
+
+
+def test_path_support_rules(lib):
+    # the generic kernel takes every valid shape, nothing takes an invalid one
+    for (M, K, N, g) in [(1, 4096, 8, -1), (3, 48, 104, 16), (5, 336, 800, 48), (1, 1, 8, 1)]:
+        assert awq.awq_path_supported(M, K, N, g, Path.GENERIC) == 1
+        assert awq.awq_select_path(M, K, N, g) in (Path.GENERIC, Path.DECODE, Path.PREFILL)
+    assert awq.awq_path_supported(1, 4096, 12, 128, Path.GENERIC) == 0
+    assert awq.awq_select_path(1, 4096, 12, 128) == -1
+    assert awq.awq_select_path(-1, 4096, 4096, 128) == -1
+    # a forced path that cannot take the shape is refused before any launch
+    for path in (Path.DECODE, Path.PREFILL):
+        if not awq.awq_path_supported(1, 4096, 8, -1, path):
+            assert fwd(M=1, K=4096, N=8, g=-1, path=path) == Status.ERR_INVALID_ARG
+
+
+def test_layer_checks_on_host():
+    qw = torch.zeros((256, 8), dtype=torch.int32)
+    qz = torch.zeros((2, 8), dtype=torch.int32)
+    sc = torch.zeros((2, 64), dtype=torch.float16)
+    layer = awq.AWQLinear(4, 128, qw, qz, sc, None)
+    assert layer.in_features == 256 and layer.out_features == 64 and layer.weight is qw
+    assert awq.AWQLinear(4, -1, qw, qz[:1], sc[:1], None).group_size == 256
+    with pytest.raises(ValueError):
+        awq.AWQLinear(8, 128, qw, qz, sc, None)
+    with pytest.raises(ValueError):
+        awq.AWQLinear(4, 100, qw, qz, sc, None)
+    with pytest.raises(ValueError):
+        awq.AWQLinear(4, 128, qw, qz[:1], sc, None)
+    with pytest.raises(ValueError):
+        awq.AWQLinear(4, 128, qw, qz, sc, torch.zeros(63, dtype=torch.float16))
+    # no CPU fallback: CPU tensors are refused loudly
+    with pytest.raises(ValueError):
+        layer(torch.zeros((1, 256), dtype=torch.float16))
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    code = ("import bit_weight_quantized_awq_gb300._binding as b\n"
+            f"b.load_library({str(tmp_path / 'nope.so')!r})\n")
+    r = subprocess.run(["python", "-c", code], cwd=ROOT, capture_output=True, text=True)
+    assert r.returncode != 0 and "not found" in r.stderr
