@@ -1,0 +1,562 @@
+"""Benchmark of the AWQ W4A16 linear forward on GB300.
+
+Metric: AWQ W4A16 GEMM throughput -- effective weight GB/s (packed weights +
+scales + zero points per call) and TFLOP/s -- with the fraction of the
+kernel's roofline.
+
+Default workload (one "step"): the decode GEMV set on 7B-class projection
+shapes, M in {1, 4, 16} x (K, N) in {(4096, 4096), (4096, 12288),
+(4096, 22016), (11008, 4096)}, group_size 128, no bias: 12 forward calls.
+Every (M, shape) call has its own weight copy (315 MB of distinct weights per
+step, more than twice the 129 MB L2), so each call reads its weights cold.
+
+    python bench.py [--steps K] [--warmup W] [--impl native|reference]
+    python bench.py --sweep --workload all    # per-problem table, every path
+
+Timing: one CUDA graph per step (its launches each bracketed by external
+event-record nodes); the timed region replays K steps between a barrier +
+synchronize on both sides; per-launch kernel durations come from the event
+nodes of the last replays. Clocks are sampled with nvidia-smi during the
+timed region. Under torchrun every rank runs the same workload on its own GPU
+(replicas, weak scaling) and rank 0 prints one JSON line with the max time
+over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "AWQ W4A16 GEMM TFLOP/s and weight GB/s vs M (1..8192), % of roofline, 1xGB300"
+
+DECODE_SHAPES = [(4096, 4096), (4096, 12288), (4096, 22016), (11008, 4096)]
+PREFILL_SHAPES = [(4096, 12288), (4096, 22016), (11008, 4096)]
+SWEEP_SHAPES = [(8192, 10240), (8192, 57344), (28672, 8192)]
+SWEEP_M = [1, 2, 4, 8, 16, 32, 64, 128, 512, 2048, 8192]
+
+WORKLOADS = {
+    # name -> list of (M, K, N, group_size, bias)
+    "decode-7b": [(M, K, N, 128, False) for M in (1, 4, 16) for (K, N) in DECODE_SHAPES],
+    "prefill-7b": [(M, K, N, 128, M != 2048) for M in (512, 2048, 8192) for (K, N) in PREFILL_SHAPES],
+    "fullrow-3d": [(2048, 4096, 4096, -1, True)],
+    "sweep-70b": [(M, K, N, 128, False) for (K, N) in SWEEP_SHAPES for M in SWEEP_M],
+}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def weight_bytes(K, N, g):
+    g = K if g == -1 else g
+    G = K // g
+    return K * N // 2 + G * N * 2 + G * N // 2
+
+
+def algo_bytes(M, K, N, g, bias):
+    """Algorithmic HBM bytes of one call: weights + scales + zeros + x + y (+ bias)."""
+    return weight_bytes(K, N, g) + 2 * M * K + 2 * M * N + (2 * N if bias else 0)
+
+
+def flops(M, K, N):
+    return 2 * M * K * N
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (replicas: no data-path collective)
+# --------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def aggregate_ranks(elapsed_s: float, units: float, device) -> tuple[float, float]:
+    """(max elapsed, summed units) over all ranks; identity without a process
+    group. The whole-job number is units of all ranks over the slowest rank."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return elapsed_s, units
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(device):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+    if device.type == "cuda":
+        torch.cuda.synchronize(device)
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
+        self.gpu_index, self.interval_ms = gpu_index, interval_ms
+        self.proc = self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.interval_ms}"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                for name, v in zip(self.NAMES, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# native arm
+# --------------------------------------------------------------------------
+
+def build_inputs(problems, device, min_bytes):
+    """Copies of the workload on the device: each copy gives every problem
+    its own weights, x, bias and y; enough copies that one pass over all of
+    them reads at least `min_bytes` of distinct weights."""
+    from bit_weight_quantized_awq_gb300.synthetic import make_activations, make_problem
+    cache = {}
+    per_step = sum(weight_bytes(K, N, g) for (M, K, N, g, b) in problems)
+    copies = max(1, -(-min_bytes // per_step))
+    sets = []
+    for _ in range(copies):
+        items = []
+        for idx, (M, K, N, g, bias) in enumerate(problems):
+            key = (K, N, g)
+            if key not in cache:
+                cache[key] = make_problem(1, K, N, g, bias=True, seed=0)
+            w = cache[key]
+            items.append({
+                "shape": (M, K, N, g, bias),
+                "x": make_activations(M, K, seed=1000 + idx).to(device),
+                "qweight": w.qweight.to(device),
+                "qzeros": w.qzeros.to(device),
+                "scales": w.scales.to(device),
+                "bias": w.bias.to(device) if bias else None,
+                "y": torch.empty((M, N), dtype=torch.float16, device=device),
+            })
+        sets.append(items)
+    return sets
+
+
+def launch(item, path, stream_handle):
+    from bit_weight_quantized_awq_gb300 import awq_linear_forward_path
+    M, K, N, g, _ = item["shape"]
+    b = item["bias"]
+    return awq_linear_forward_path(item["x"].data_ptr(), item["qweight"].data_ptr(),
+                                   item["qzeros"].data_ptr(), item["scales"].data_ptr(),
+                                   None if b is None else b.data_ptr(), item["y"].data_ptr(),
+                                   M, K, N, g, stream_handle, int(path))
+
+
+def capture_step(items, path, stream, with_events=True):
+    """One CUDA graph for one pass over `items`; returns (graph, event pairs)."""
+    handle = stream.cuda_stream
+    evs = []
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for it in items:
+            if with_events:
+                e0 = torch.cuda.Event(enable_timing=True, external=True)
+                e1 = torch.cuda.Event(enable_timing=True, external=True)
+                e0.record(stream)
+            st = launch(it, path, handle)
+            if st != 0:
+                raise RuntimeError(f"launch failed with status {st} for {it['shape']}")
+            if with_events:
+                e1.record(stream)
+                evs.append((e0, e1))
+    return graph, evs
+
+
+def run_native(args, problems, device):
+    import bit_weight_quantized_awq_gb300 as awq
+    from bit_weight_quantized_awq_gb300 import Path
+    awq.load_library()
+    path = Path[args.path.upper()]
+    sets = build_inputs(problems, device, 2 * L2_BYTES)
+    stream = torch.cuda.Stream(device)
+    handle = stream.cuda_stream
+    # eager pass first: allocates the per-stream scratch area before capture
+    with torch.cuda.stream(stream):
+        for items in sets:
+            for it in items:
+                st = launch(it, path, handle)
+                if st != 0:
+                    raise RuntimeError(f"status {st} for {it['shape']}")
+    stream.synchronize()
+    st = awq.awq_last_device_status(handle)
+    if st != 0:
+        raise RuntimeError(awq.awq_status_string(st))
+
+    use_events = True
+    try:
+        graphs = [capture_step(items, path, stream, True) for items in sets]
+    except Exception:
+        use_events = False
+        graphs = [capture_step(items, path, stream, False) for items in sets]
+    for i in range(args.warmup):
+        graphs[i % len(graphs)][0].replay()
+    torch.cuda.synchronize(device)
+
+    ws, rank, local = dist_env()
+    barrier(device)
+    with ClockSampler(torch.cuda.current_device() if ws == 1 else local) as clk:
+        barrier(device)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            graphs[i % len(graphs)][0].replay()
+        end.record(stream)
+        barrier(device)
+    elapsed = start.elapsed_time(end) / 1e3
+    clocks = clk.summary()
+
+    st = awq.awq_last_device_status(handle)
+    if st != 0:
+        raise RuntimeError(awq.awq_status_string(st))
+
+    wbytes = sum(weight_bytes(K, N, g) for (M, K, N, g, b) in problems)
+    fl = sum(flops(M, K, N) for (M, K, N, g, b) in problems)
+    abytes = sum(algo_bytes(*p) for p in problems)
+    max_el, tot_wbytes = aggregate_ranks(elapsed, wbytes * args.steps, device)
+    _, tot_flops = aggregate_ranks(elapsed, fl * args.steps, device)
+
+    per_problem = None
+    if use_events:
+        per_problem = [[] for _ in problems]
+        for (_, evs) in graphs:
+            for j, (e0, e1) in enumerate(evs):
+                per_problem[j].append(e0.elapsed_time(e1) / 1e3)
+    return {"elapsed": max_el, "tot_wbytes": tot_wbytes, "tot_flops": tot_flops,
+            "wbytes": wbytes, "flops": fl, "abytes": abytes, "clocks": clocks,
+            "per_problem": per_problem, "copies": len(sets), "graph_events": use_events,
+            "launches": args.steps * len(problems), "sets": sets}
+
+
+def run_e2e(args, problems, device, sets, steps):
+    """The same metric through the public torch API from host buffers: every
+    step copies x from pinned host memory, runs the layer, reads y back."""
+    from bit_weight_quantized_awq_gb300 import Path, linear_forward
+    items = sets[0]
+    xh = [it["x"].cpu().pin_memory() for it in items]
+    yh = [torch.empty(it["y"].shape, dtype=torch.float16).pin_memory() for it in items]
+    xd = [torch.empty_like(it["x"]) for it in items]
+    path = Path[args.path.upper()]
+    h2d = sum(x.numel() * 2 for x in xh)
+    d2h = sum(y.numel() * 2 for y in yh)
+
+    def one_step():
+        for j, it in enumerate(items):
+            xd[j].copy_(xh[j], non_blocking=True)
+            y = linear_forward(xd[j], it["qweight"], it["qzeros"], it["scales"], it["bias"],
+                               it["shape"][3], path=path)
+            yh[j].copy_(y, non_blocking=True)
+
+    for _ in range(max(3, args.warmup // 10)):
+        one_step()
+    barrier(device)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one_step()
+    barrier(device)
+    return time.perf_counter() - t0, h2d, d2h
+
+
+# --------------------------------------------------------------------------
+# oracle (CPU baseline and reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_step(problems, cache, col_words=None, which=None):
+    """The oracle on the problems (all of them, or only index `which`), over
+    all columns or the first `col_words` packed words. Returns the weight
+    bytes it processed."""
+    import numpy as np
+    import oracle
+    from bit_weight_quantized_awq_gb300.synthetic import make_activations, make_problem
+    done = 0
+    for idx in (range(len(problems)) if which is None else [which]):
+        M, K, N, g, bias = problems[idx]
+        key = (K, N, g)
+        if key not in cache:
+            w = make_problem(1, K, N, g, bias=True, seed=0)
+            cache[key] = (w.qweight.numpy(), w.qzeros.numpy(), w.scales.numpy(), w.bias.numpy())
+        if ("x", idx) not in cache:
+            cache[("x", idx)] = make_activations(M, K, seed=1000 + idx).numpy()
+        qw, qz, sc, b = cache[key]
+        n_words = N // 8 if col_words is None else min(col_words, N // 8)
+        skey = ("slice", key, n_words)
+        if skey not in cache:
+            cache[skey] = (np.ascontiguousarray(qw[:, :n_words]), np.ascontiguousarray(qz[:, :n_words]),
+                           np.ascontiguousarray(sc[:, :8 * n_words]), np.ascontiguousarray(b[:8 * n_words]))
+        qws, qzs, scs, bs = cache[skey]
+        oracle.forward(cache[("x", idx)], qws, qzs, scs, bs if bias else None, g)
+        done += weight_bytes(K, 8 * n_words, g)
+    return done
+
+
+def cpu_baseline(problems, budget_s=12.0):
+    """The oracle on whole steps of the workload (every problem, every row and
+    column), repeated until about `budget_s` has passed; weight GB/s."""
+    import oracle
+    oracle.build()
+    cache = {}
+    oracle_step(problems, cache, col_words=1)   # input generation stays outside the timing
+    t0 = time.perf_counter()
+    done, steps = 0, 0
+    while True:
+        done += oracle_step(problems, cache)
+        steps += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"value": done / el / 1e9, "unit": "weight GB/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{steps} full step(s) of the workload ({len(problems)} problems, all rows "
+                      f"and columns), fp64 oracle on {os.cpu_count()} threads, {el:.1f} s"}
+
+
+def run_reference(args, problems):
+    """--impl reference: the oracle on this workload, timed on the host
+    cores. Each step is one problem (in rotation) over its first 8 packed
+    words (64 output columns), so that K + W steps end within minutes."""
+    import oracle
+    oracle.build()
+    cache = {}
+    for i in range(len(problems)):
+        oracle_step(problems, cache, col_words=8, which=i)
+    for i in range(args.warmup):
+        oracle_step(problems, cache, col_words=8, which=i % len(problems))
+    t0 = time.perf_counter()
+    done = 0
+    for i in range(args.steps):
+        done += oracle_step(problems, cache, col_words=8, which=i % len(problems))
+    el = time.perf_counter() - t0
+    value = done / el / 1e9
+    sample = (f"each step: one of the {len(problems)} problems in rotation, all rows, first 64 "
+              f"output columns; fp64 oracle on {os.cpu_count()} threads")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "weight GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "problems": len(problems)},
+        "cpu_baseline": {"value": value, "unit": "weight GB/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "weight GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# --------------------------------------------------------------------------
+# sweep: per-problem table of every path that can take the shape
+# --------------------------------------------------------------------------
+
+def run_sweep(args, device, peaks):
+    import bit_weight_quantized_awq_gb300 as awq
+    from bit_weight_quantized_awq_gb300 import Path
+    awq.load_library()
+    out = open(args.sweep_out, "w") if args.sweep_out else None
+    names = list(WORKLOADS) if args.workload == "all" else [args.workload]
+    stream = torch.cuda.Stream(device)
+    handle = stream.cuda_stream
+    for wl in names:
+        for prob in WORKLOADS[wl]:
+            M, K, N, g, bias = prob
+            for path in (Path.DECODE, Path.PREFILL, Path.GENERIC):
+                if not awq.awq_path_supported(M, K, N, g, path):
+                    continue
+                if path == Path.GENERIC and flops(M, K, N) > 2e11:
+                    continue
+                sets = build_inputs([prob], device, 2 * L2_BYTES)
+                with torch.cuda.stream(stream):
+                    for s in sets:
+                        launch(s[0], path, handle)
+                stream.synchronize()
+                reps = max(3, min(200, int(2e-3 / max(1e-7, flops(M, K, N) / 1e15))))
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=stream):
+                    for r in range(reps):
+                        launch(sets[r % len(sets)][0], path, handle)
+                graph.replay()
+                torch.cuda.synchronize(device)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                torch.cuda.synchronize(device)
+                t = e0.elapsed_time(e1) / 1e3 / reps
+                row = {"workload": wl, "M": M, "K": K, "N": N, "g": g, "bias": bias,
+                       "path": path.name.lower(), "us": t * 1e6,
+                       "tflops": flops(M, K, N) / t / 1e12,
+                       "weight_gbs": weight_bytes(K, N, g) / t / 1e9,
+                       "hbm_frac": algo_bytes(*prob) / t / 1e9 / peaks["hbm_gbs"],
+                       "tc_frac": flops(M, K, N) / t / 1e12 / peaks["bf16_tflops"]}
+                print(json.dumps(row), file=sys.stderr, flush=True)
+                if out:
+                    out.write(json.dumps(row) + "\n")
+                    out.flush()
+                del sets, graph
+                torch.cuda.empty_cache()
+    if out:
+        out.close()
+
+
+# --------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="decode-7b", choices=list(WORKLOADS) + ["all"])
+    ap.add_argument("--path", default="auto", choices=["auto", "generic", "decode", "prefill"])
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--sweep-out", default=None)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, WORKLOADS[args.workload if args.workload != "all" else "decode-7b"])
+        return
+
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", torch.cuda.current_device())
+    peaks = load_peaks()
+
+    if args.sweep:
+        run_sweep(args, device, peaks)
+        return
+
+    problems = WORKLOADS[args.workload]
+    r = run_native(args, problems, device)
+    e2e_el, h2d, d2h = run_e2e(args, problems, device, r["sets"], args.e2e_steps)
+    e2e_el, e2e_units = aggregate_ranks(e2e_el, r["wbytes"] * args.e2e_steps, device)
+
+    import bit_weight_quantized_awq_gb300 as awq
+    paths = [awq.awq_select_path(p[0], p[1], p[2], p[3]) for p in problems]
+    roof, per = None, None
+    if r["per_problem"]:
+        avg = [statistics.mean(ts) for ts in r["per_problem"]]
+        kernel_time = sum(avg)
+        achieved = r["abytes"] / kernel_time / 1e9
+        names = {1: "generic_forward_kernel", 2: "decode_kernel<MT>", 3: "prefill kernel"}
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
+                "kernel": names.get(max(set(paths), key=paths.count), "?"),
+                "bytes_per_launch_avg": r["abytes"] / len(problems),
+                "launch_us_avg": kernel_time / len(problems) * 1e6}
+        per = [{"M": p[0], "K": p[1], "N": p[2], "us": round(a * 1e6, 3),
+                "hbm_frac": round(algo_bytes(*p) / a / 1e9 / peaks["hbm_gbs"], 4),
+                "weight_gbs": round(weight_bytes(p[1], p[2], p[3]) / a / 1e9, 1)}
+               for p, a in zip(problems, avg)]
+
+    line = {
+        "metric": METRIC, "value": r["tot_wbytes"] / r["elapsed"] / 1e9, "unit": "weight GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": r["elapsed"] / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "problems": len(problems),
+                   "shapes_M_K_N_g_bias": [list(p) for p in problems], "path": args.path,
+                   "paths_auto": paths,
+                   "l2": f"inputs larger than L2: {r['copies']} weight copies, "
+                         f"{r['wbytes'] * r['copies'] / 2**20:.0f} MiB of distinct weights",
+                   "parallelism": f"replicas x{ws}",
+                   "timing": "CUDA graph per step, CUDA events (external event nodes per launch)"},
+        "tflops": r["tot_flops"] / r["elapsed"] / 1e12,
+        "roofline": roof,
+        "per_problem": per,
+        "e2e": {"value": e2e_units / e2e_el / 1e9, "unit": "weight GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "bit_weight_quantized_awq_gb300.linear_forward, eager, pinned host x/y"},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(problems)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

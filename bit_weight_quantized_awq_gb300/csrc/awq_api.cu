@@ -195,16 +195,16 @@ awq_status_t awq_linear_forward_path(const void *x, const int32_t *qweight, cons
     if (M < 0) return AWQ_ERR_INVALID_ARG;
     awq_status_t st = check_shape(K, N, group_size, &g);
     if (st != AWQ_OK) return st;
+    if (path != AWQ_PATH_AUTO && path != AWQ_PATH_GENERIC && path != AWQ_PATH_DECODE &&
+        path != AWQ_PATH_PREFILL)
+        return AWQ_ERR_INVALID_ARG;
+    if (M == 0) return AWQ_OK;   // empty x and y may be NULL; nothing to do
     if (!x || !qweight || !qzeros || !scales || !y) return AWQ_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(qweight) || !aligned16(qzeros) || !aligned16(scales) ||
         !aligned16(y) || (bias && !aligned16(bias)))
         return AWQ_ERR_MISALIGNED;
-    if (path != AWQ_PATH_AUTO && path != AWQ_PATH_GENERIC && path != AWQ_PATH_DECODE &&
-        path != AWQ_PATH_PREFILL)
-        return AWQ_ERR_INVALID_ARG;
     Problem p{x, qweight, qzeros, scales, bias, y, M, K, N, g, K / g};
     if (path != AWQ_PATH_AUTO && !path_fits(p, path)) return AWQ_ERR_INVALID_ARG;
-    if (M == 0) return AWQ_OK;
     const awq_path_t use = (path == AWQ_PATH_AUTO) ? auto_path(p) : path;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;

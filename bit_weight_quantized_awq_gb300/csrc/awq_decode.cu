@@ -1,6 +1,584 @@
-// awq_decode.cu -- decode path (small M). Not built yet: reports unsupported.
+// awq_decode.cu -- decode path of the WQLinear forward (small M, 1..16 rows).
+//
+// Predibase Lorax "AWQ WQLinear" page, Description, forward steps 2-3:
+//   y[m, n] = fp16_rn( sum_k x[m, k] * W[k, n] + bias[n] ),
+//   W[k, n] = fp16_rn((q[k, n] - z[k/g, n]) * s[k/g, n]), fp32 accumulation.
+//
+// At small M the layer is bound by streaming the packed weights from HBM
+// (0.52 bytes per weight at g = 128). The kernel is built around that:
+//
+//  * Work: the K x N weight matrix is cut into tiles of 256 columns (one
+//    128-byte row of packed words) and stage blocks of 64 k-rows. The
+//    (tile, block) iterations, tile-major, are split evenly between the CTAs
+//    (one per SM): each CTA streams a contiguous run of them ("stream-K").
+//  * Loads: one producer warp issues 2-D TMA boxes per stage -- 64 x 128 B of
+//    qweight (128-byte swizzle), the 64 x Mpad activation slice, and the
+//    scale and zero-point rows of the groups the stage touches -- into an
+//    8-stage ring guarded by mbarriers (full: TMA bytes landed; empty: the
+//    consumers released the slot).
+//  * Math: 8 consumer warps (two groups of four that take alternate stages;
+//    each warp owns 64 columns) dequantise in registers and run the
+//    legacy-path tensor-core MMA m16n8k16 with W as the A operand (16 output
+//    columns x 16 k) and the activations as B (16 k x 8 tokens), fp32
+//    accumulators. Two k-adjacent weights of one column form one half2
+//    operand register: a byte permute brings byte b of rows k and k+1
+//    together, one LOP3 masks a nibble into the fraction of 1024.0 or 64.0,
+//    an exact half2 subtract removes the zero point and one half2 multiply
+//    (round to nearest) applies the scale -- exactly fp16_rn((q - z) s).
+//  * Reduction: a tile split between CTAs is summed by its contributors
+//    together at the end of the kernel: each writes its fp32 partial to
+//    scratch and counts itself in; after its own stream is done it waits
+//    (bounded) for the count and then reduces a slice of the tile, in the
+//    fixed contributor order, adding the bias and rounding once. The grid is
+//    launched cooperatively so that every CTA is resident.
+//
+// Requirements (else the generic kernel serves): 1 <= M <= 16, K % 16 == 0,
+// N % 32 == 0 (TMA row pitch), g % 16 == 0, base pointers 16-byte aligned.
+#include <algorithm>
+#include <map>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "awq_device.cuh"
 #include "awq_internal.h"
+
 namespace awq {
-bool decode_supported(int64_t, int64_t, int64_t, int64_t) { return false; }
-cudaError_t launch_decode(const Problem &, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int kTileWords = 32;   // packed words per tile row
+constexpr int kTileCols = 256;   // output columns per tile
+constexpr int kStageRows = 64;   // k-rows per pipeline stage
+constexpr int kStages = 8;
+constexpr int kColWarps = 4;     // warps across a tile's columns, 8 words each
+constexpr int kKGroups = 2;      // consumer groups taking alternate stages
+constexpr int kConsumerWarps = kColWarps * kKGroups;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr int kMaxTokens = 16;
+constexpr int kMaxGroupRows = 5; // group rows one 64-row stage can touch when g >= 16
+
+constexpr int kWBytes = kStageRows * 128;
+constexpr int kXBytes = kMaxTokens * 128;
+constexpr int kSBytes = kMaxGroupRows * kTileCols * 2;
+constexpr int kZBytes = kMaxGroupRows * kTileWords * 4;
+constexpr int kXOff = kWBytes;
+constexpr int kSOff = kXOff + kXBytes;
+constexpr int kZOff = kSOff + kSBytes;
+constexpr int kStageBytes = 14 * 1024;
+static_assert(kZOff + kZBytes <= kStageBytes, "stage layout overflows");
+static_assert(kStageBytes % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+constexpr int kRedOff = kStages * kStageBytes;
+constexpr int kRedBytes = kMaxTokens * kTileCols * 4;
+constexpr int kBarOff = kRedOff + kRedBytes;
+constexpr int kSmemBytes = kBarOff + 256 + 1024;   // barriers + flags + alignment slack
+
+constexpr int kPartialFloats = kMaxTokens * kTileCols;  // one partial slot
+
+struct DecodeParams {
+    const __half *bias;
+    __half *y;
+    float *partials;        // [2 * ctas][16][256]
+    unsigned int *arrive;   // [tiles]
+    unsigned int *depart;   // [tiles]
+    unsigned int *status;
+    int M, K, N, g;
+    int tiles, kiters, total, ctas;
+    uint32_t stage_tx;      // bytes one stage's TMA boxes deliver
+};
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
+    __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+
+__device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
+    __half2 r = __hmul2_rn(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+
+// The CTA whose iteration range contains iteration `it`.
+__device__ __forceinline__ int cta_of(int it, int total, int ctas) {
+    return (int)((((int64_t)it + 1) * ctas - 1) / total);
+}
+__device__ __forceinline__ int range_begin(int c, int total, int ctas) {
+    return (int)(((int64_t)c * total) / ctas);
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+              const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
+              const DecodeParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    float *red = reinterpret_cast<float *>(smem + kRedOff);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kBarOff);
+    uint64_t *empty = full + kStages;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStages);
+    volatile int *duty_ok = abort_flag + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int c = blockIdx.x;
+    const int begin = range_begin(c, p.total, p.ctas);
+    const int end = range_begin(c + 1, p.total, p.ctas);
+    const int n_iters = end - begin;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(ptx::smem_addr(full + s), 1);
+            ptx::mbar_init(ptx::smem_addr(empty + s), kColWarps);
+        }
+        *abort_flag = 0;
+        *duty_ok = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------------ producer
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            ptx::prefetch_tmap(&tm_w);
+            ptx::prefetch_tmap(&tm_x);
+            ptx::prefetch_tmap(&tm_s);
+            ptx::prefetch_tmap(&tm_z);
+            int issued = 0;
+            for (int i = 0; i < n_iters; ++i) {
+                const int it = begin + i;
+                const int tile = it / p.kiters;
+                const int kb = it - tile * p.kiters;
+                const int s = i % kStages;
+                const uint32_t parity = ((i / kStages) & 1) ^ 1;
+                if (!ptx::mbar_wait_bounded(ptx::smem_addr(empty + s), parity, abort_flag, p.status))
+                    break;
+                const uint32_t fb = ptx::smem_addr(full + s);
+                const uint32_t st = ptx::smem_addr(smem + s * kStageBytes);
+                const int k0 = kb * kStageRows;
+                ptx::mbar_arrive_expect_tx(fb, p.stage_tx);
+                ptx::tma_load_2d(st, &tm_w, fb, tile * kTileWords, k0);
+                ptx::tma_load_2d(st + kXOff, &tm_x, fb, k0, 0);
+                ptx::tma_load_2d(st + kSOff, &tm_s, fb, tile * kTileCols, k0 / p.g);
+                ptx::tma_load_2d(st + kZOff, &tm_z, fb, tile * kTileWords, k0 / p.g);
+                issued = i + 1;
+            }
+            if (*abort_flag) {
+                // let the copies already in flight land before the CTA exits
+                for (int i = std::max(0, issued - kStages); i < issued; ++i)
+                    ptx::mbar_wait_bounded(ptx::smem_addr(full + i % kStages), (i / kStages) & 1,
+                                           nullptr, nullptr);
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------------ consumers
+    const int kg = warp / kColWarps;   // which alternate-stage group
+    const int cw = warp % kColWarps;   // which 64-column quarter of the tile
+    const int gq = lane >> 2;          // MMA groupID: output column pair / token
+    const int tq = lane & 3;           // MMA thread-in-group: k pair / token pair
+    const int word = cw * 8 + gq;      // packed word (8 columns) this thread owns
+    const int ct = cw * 32 + lane;     // thread index within a group
+
+    float acc[4][MT][4];
+    uint32_t S2[8], Zlo[4], Zhi[4];
+    int cur_group = -1;
+    int seg_kb0 = 0;
+    int duty_tiles[2] = {-1, -1};
+    const int first_tile = begin / p.kiters;
+
+    for (int i = 0; i < n_iters; ++i) {
+        const int it = begin + i;
+        const int tile = it / p.kiters;
+        const int kb = it - tile * p.kiters;
+        if (i == 0 || kb == 0) {
+            seg_kb0 = kb;
+            cur_group = -1;
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[b][mt][e] = 0.f;
+        }
+        if ((i & 1) == kg) {
+            const int s = i % kStages;
+            // every lane waits (each needs the acquire); the MMA below is
+            // warp-wide, so the outcome is made uniform across the warp
+            const bool ok = __all_sync(0xffffffffu,
+                                       ptx::mbar_wait_bounded(ptx::smem_addr(full + s), (i / kStages) & 1,
+                                                              abort_flag, p.status));
+            if (ok) {
+                const uint32_t wbase = ptx::smem_addr(smem + s * kStageBytes);
+                const uint32_t xbase = wbase + kXOff;
+                const uint32_t sbase = wbase + kSOff;
+                const uint32_t zbase = wbase + kZOff;
+                const int k0 = kb * kStageRows;
+                const int grp0 = k0 / p.g;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    const int kc = k0 + 16 * ch;
+                    if (kc >= p.K) break;
+                    const int grp = kc / p.g;
+                    if (grp != cur_group) {
+                        cur_group = grp;
+                        const int r = grp - grp0;
+                        uint4 sv;
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(sv.x), "=r"(sv.y), "=r"(sv.z), "=r"(sv.w)
+                                     : "r"(sbase + r * (kTileCols * 2) + word * 16));
+                        const uint32_t zw = lds32(zbase + r * (kTileWords * 4) + word * 4);
+                        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            S2[2 * h] = __byte_perm(sw[h], sw[h], 0x1010);
+                            S2[2 * h + 1] = __byte_perm(sw[h], sw[h], 0x3232);
+                        }
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            const uint32_t t = __byte_perm(zw, zw, b | ((4 + b) << 8));
+                            Zlo[b] = (t & 0x000F000Fu) | 0x64006400u;
+                            Zhi[b] = (t & 0x00F000F0u) | 0x54005400u;
+                        }
+                    }
+                    // packed words of rows 16ch + 2tq (+1, +8, +9), 128-byte swizzle
+                    const int r0 = 16 * ch + 2 * tq;
+                    const uint32_t chunk = (uint32_t)(word >> 2);
+                    const uint32_t inw = (uint32_t)(word & 3) * 4;
+                    auto waddr = [&](int r) {
+                        return wbase + r * 128 + ((chunk ^ (uint32_t)(r & 7)) << 4) + inw;
+                    };
+                    const uint32_t v0 = lds32(waddr(r0));
+                    const uint32_t v1 = lds32(waddr(r0 + 1));
+                    const uint32_t v8 = lds32(waddr(r0 + 8));
+                    const uint32_t v9 = lds32(waddr(r0 + 9));
+                    uint32_t bf[MT][2];
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        const int xr = 8 * mt + gq;
+                        bf[mt][0] = lds32(xbase + xr * 128 + (((uint32_t)(2 * ch) ^ (uint32_t)(xr & 7)) << 4) + 4 * tq);
+                        bf[mt][1] = lds32(xbase + xr * 128 + (((uint32_t)(2 * ch + 1) ^ (uint32_t)(xr & 7)) << 4) + 4 * tq);
+                    }
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        const uint32_t sel = (uint32_t)(b | ((4 + b) << 8));
+                        const uint32_t t01 = __byte_perm(v0, v1, sel);
+                        const uint32_t t89 = __byte_perm(v8, v9, sel);
+                        uint32_t a[4];
+                        a[0] = hmul2_u(hsub2_u((t01 & 0x000F000Fu) | 0x64006400u, Zlo[b]), S2[2 * b]);
+                        a[1] = hmul2_u(hsub2_u((t01 & 0x00F000F0u) | 0x54005400u, Zhi[b]), S2[2 * b + 1]);
+                        a[2] = hmul2_u(hsub2_u((t89 & 0x000F000Fu) | 0x64006400u, Zlo[b]), S2[2 * b]);
+                        a[3] = hmul2_u(hsub2_u((t89 & 0x00F000F0u) | 0x54005400u, Zhi[b]), S2[2 * b + 1]);
+#pragma unroll
+                        for (int mt = 0; mt < MT; ++mt) ptx::mma_16816(acc[b][mt], a, bf[mt][0], bf[mt][1]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(empty + s));
+        }
+
+        if (i == n_iters - 1 || kb == p.kiters - 1) {
+            // ---- segment end: fold the second group's sums into the first's
+            if (kg == 1) {
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) red[(b * MT + mt) * 512 + e * 128 + ct] = acc[b][mt][e];
+            }
+            ptx::named_barrier(1, kConsumerThreads);
+            if (kg == 0) {
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[b][mt][e] += red[(b * MT + mt) * 512 + e * 128 + ct];
+            }
+            ptx::named_barrier(1, kConsumerThreads);
+
+            // `whole` is uniform across the CTA; barrier participation never
+            // depends on the abort flag, which other warps may set at any time
+            const bool whole = (seg_kb0 == 0 && kb == p.kiters - 1);
+            if (kg == 0) {
+                const bool live = !*abort_flag;
+                const int col0 = tile * kTileCols + word * 8;
+                if (whole && live) {
+                    float bv[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) bv[j] = 0.f;
+                    if (p.bias && col0 < p.N) {
+                        const uint4 braw = *reinterpret_cast<const uint4 *>(p.bias + col0);
+                        const __half *bh = reinterpret_cast<const __half *>(&braw);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) bv[j] = __half2float(bh[j]);
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int m = 8 * mt + 2 * tq + e;
+                            if (m < p.M && col0 < p.N) {
+                                __align__(16) __half out[8];
+#pragma unroll
+                                for (int b = 0; b < 4; ++b) {
+                                    out[2 * b] = __float2half_rn(acc[b][mt][e] + bv[2 * b]);
+                                    out[2 * b + 1] = __float2half_rn(acc[b][mt][2 + e] + bv[2 * b + 1]);
+                                }
+                                *reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.N + col0) =
+                                    *reinterpret_cast<const uint4 *>(out);
+                            }
+                        }
+                } else if (!whole && live) {
+                    const int which = (tile == first_tile) ? 0 : 1;
+                    float *slot = p.partials + (int64_t)(2 * c + which) * kPartialFloats;
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int m = 8 * mt + 2 * tq + e;
+                            if (m < p.M) {
+                                float4 lo = make_float4(acc[0][mt][e], acc[0][mt][2 + e], acc[1][mt][e], acc[1][mt][2 + e]);
+                                float4 hi = make_float4(acc[2][mt][e], acc[2][mt][2 + e], acc[3][mt][e], acc[3][mt][2 + e]);
+                                float4 *dst = reinterpret_cast<float4 *>(slot + m * kTileCols + word * 8);
+                                dst[0] = lo;
+                                dst[1] = hi;
+                            }
+                        }
+                    __threadfence();
+                }
+                if (!whole) {
+                    ptx::named_barrier(2, kConsumerThreads / kKGroups);
+                    if (ct == 0 && !*abort_flag) atomicAdd(p.arrive + tile, 1u);
+                }
+            }
+            if (!whole) duty_tiles[duty_tiles[0] < 0 ? 0 : 1] = tile;
+        }
+    }
+
+    // ---- reduction duties: every split tile this CTA helped with
+    const int ctid = threadIdx.x;   // 0 .. kConsumerThreads-1
+#pragma unroll 1
+    for (int d = 0; d < 2; ++d) {
+        const int t = duty_tiles[d];
+        if (t < 0) break;
+        const int cf = cta_of(t * p.kiters, p.total, p.ctas);
+        const int cl = cta_of((t + 1) * p.kiters - 1, p.total, p.ctas);
+        const int n = cl - cf + 1;
+        if (ctid == 0) {
+            bool ok = !*abort_flag;
+            if (ok) {
+                const uint64_t t0 = ptx::globaltimer();
+                while (ptx::ld_acquire_gpu(p.arrive + t) < (unsigned)n) {
+                    if (*abort_flag || ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+                        ok = false;
+                        *abort_flag = 1;
+                        atomicOr(p.status, kStatusTimeout);
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+            *duty_ok = ok ? 1 : 0;
+        }
+        ptx::named_barrier(1, kConsumerThreads);
+        if (*duty_ok) {
+            const int units = p.M * kTileWords;          // (token, word) pairs of the tile
+            const int i = c - cf;
+            const int u0 = (int)((int64_t)i * units / n);
+            const int u1 = (int)((int64_t)(i + 1) * units / n);
+            for (int u = u0 + ctid; u < u1; u += kConsumerThreads) {
+                const int m = u / kTileWords;
+                const int w = u - m * kTileWords;
+                const int col0 = t * kTileCols + w * 8;
+                if (col0 >= p.N) continue;
+                float s8[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) s8[j] = 0.f;
+                for (int cc = cf; cc <= cl; ++cc) {
+                    const int which = (t == range_begin(cc, p.total, p.ctas) / p.kiters) ? 0 : 1;
+                    const float4 *src = reinterpret_cast<const float4 *>(
+                        p.partials + (int64_t)(2 * cc + which) * kPartialFloats + m * kTileCols + w * 8);
+                    const float4 lo = __ldcg(src), hi = __ldcg(src + 1);
+                    s8[0] += lo.x; s8[1] += lo.y; s8[2] += lo.z; s8[3] += lo.w;
+                    s8[4] += hi.x; s8[5] += hi.y; s8[6] += hi.z; s8[7] += hi.w;
+                }
+                __align__(16) __half out[8];
+                if (p.bias) {
+                    const uint4 braw = *reinterpret_cast<const uint4 *>(p.bias + col0);
+                    const __half *bh = reinterpret_cast<const __half *>(&braw);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) out[j] = __float2half_rn(s8[j] + __half2float(bh[j]));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) out[j] = __float2half_rn(s8[j]);
+                }
+                *reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.N + col0) = *reinterpret_cast<const uint4 *>(out);
+            }
+        }
+        ptx::named_barrier(1, kConsumerThreads);
+        if (ctid == 0 && *duty_ok) {
+            // last one out resets the tile's counters for the next call
+            if (atomicAdd(p.depart + t, 1u) == (unsigned)(n - 1)) {
+                atomicExch(p.arrive + t, 0u);
+                atomicExch(p.depart + t, 0u);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
+                 uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
+                 CUtensorMapSwizzle swizzle)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Largest number of groups one 64-row stage can touch.
+int group_rows_per_stage(int64_t g)
+{
+    if (kStageRows % g == 0) return (int)(kStageRows / g);
+    if (g % kStageRows == 0) return 1;
+    return (int)((kStageRows - 1) / g + 2);
+}
+
+// Per (device, kernel variant): dynamic shared memory opted in once, and the
+// number of resident CTAs per SM with the SM count.
+struct LaunchInfo {
+    int occ = 0;
+    int sms = 0;
+    cudaError_t err = cudaSuccess;
+};
+
+template <int MT>
+LaunchInfo launch_info()
+{
+    static std::mutex mu;
+    static std::map<int, LaunchInfo> cache;
+    int dev = 0;
+    LaunchInfo li;
+    li.err = cudaGetDevice(&dev);
+    if (li.err != cudaSuccess) return li;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    auto kern = decode_kernel<MT>;
+    li.err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (li.err == cudaSuccess)
+        li.err = cudaDeviceGetAttribute(&li.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (li.err == cudaSuccess)
+        li.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&li.occ, kern, kThreads, kSmemBytes);
+    if (li.err == cudaSuccess && li.occ < 1) li.err = cudaErrorLaunchOutOfResources;
+    if (li.err == cudaSuccess) cache[dev] = li;
+    return li;
+}
+
+template <int MT>
+cudaError_t launch_decode_t(const Problem &pr, cudaStream_t stream)
+{
+    const LaunchInfo li = launch_info<MT>();
+    if (li.err != cudaSuccess) return li.err;
+
+    const int M = (int)pr.M, K = (int)pr.K, N = (int)pr.N, g = (int)pr.g;
+    const int tiles = (N + kTileCols - 1) / kTileCols;
+    const int kiters = (K + kStageRows - 1) / kStageRows;
+    const int64_t total = (int64_t)tiles * kiters;
+    const int ctas = (int)std::min<int64_t>(total, (int64_t)li.occ * li.sms);
+    const int R = group_rows_per_stage(g);
+    const int mpad = 8 * MT;
+
+    Scratch sc{};
+    if (!get_scratch(stream, (size_t)2 * ctas * kPartialFloats, (size_t)2 * tiles, &sc))
+        return cudaErrorMemoryAllocation;
+
+    CUtensorMap tw, tx, ts, tz;
+    bool ok = make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_INT32, pr.qweight, N / 8, K, (uint64_t)N / 2,
+                          kTileWords, kStageRows, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.x, K, M, (uint64_t)K * 2,
+                          kStageRows, mpad, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.scales, N, pr.G, (uint64_t)N * 2,
+                          kTileCols, R, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              make_map_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_INT32, pr.qzeros, N / 8, pr.G, (uint64_t)N / 2,
+                          kTileWords, R, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!ok) return cudaErrorInvalidValue;
+
+    DecodeParams p{};
+    p.bias = static_cast<const __half *>(pr.bias);
+    p.y = static_cast<__half *>(pr.y);
+    p.partials = sc.partials;
+    p.arrive = sc.counters;
+    p.depart = sc.counters + tiles;
+    p.status = device_status_word();
+    p.M = M; p.K = K; p.N = N; p.g = g;
+    p.tiles = tiles; p.kiters = kiters; p.total = (int)total; p.ctas = ctas;
+    p.stage_tx = (uint32_t)(kWBytes + mpad * 128 + R * (kTileCols * 2) + R * (kTileWords * 4));
+
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<MT>, tw, tx, ts, tz, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+} // namespace
+
+bool decode_supported(int64_t M, int64_t K, int64_t N, int64_t g)
+{
+    return M >= 1 && M <= kMaxTokens && K % 16 == 0 && N % 32 == 0 && g % 16 == 0 &&
+           K <= (int64_t(1) << 30) && N <= (int64_t(1) << 30) &&
+           ((K + kStageRows - 1) / kStageRows) * ((N + kTileCols - 1) / kTileCols) < (int64_t(1) << 31);
+}
+
+cudaError_t launch_decode(const Problem &p, cudaStream_t stream)
+{
+    if (!decode_supported(p.M, p.K, p.N, p.g)) return cudaErrorInvalidValue;
+    return p.M <= 8 ? launch_decode_t<1>(p, stream) : launch_decode_t<2>(p, stream);
+}
+
 } // namespace awq

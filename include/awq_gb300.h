@@ -82,7 +82,8 @@ typedef enum {
  *   scales     fp16 [G, N]                      (read)
  *   bias       fp16 [N], or NULL for no bias    (read)
  *   y          fp16 [M, N]                      (written; must not alias inputs)
- *   M          rows of x; M == 0 returns AWQ_OK and enqueues nothing
+ *   M          rows of x; M == 0 returns AWQ_OK and enqueues nothing once K, N and
+ *              group_size pass their rules (x and y may then be NULL)
  *   K, N       in_features, out_features (N % 8 == 0)
  *   group_size g > 0 with K % g == 0, or -1 for g = K
  *   stream     CUDA stream to enqueue on
