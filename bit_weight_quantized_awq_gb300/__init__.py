@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     awq_dequant,
     awq_last_device_status,
     awq_linear_forward,
+    awq_linear_forward_decode_noalloc,
     awq_linear_forward_path,
     awq_path_supported,
     awq_select_path,

@@ -25,6 +25,7 @@ EXPORTED = (
     "awq_status_string",
     "awq_last_device_status",
     "awq_shutdown",
+    "awq_linear_forward_decode_noalloc",
 )
 
 
@@ -34,6 +35,7 @@ class Status(enum.IntEnum):
     ERR_MISALIGNED = 2
     ERR_CUDA = 3
     ERR_TIMEOUT = 4
+    ERR_TOO_LARGE = 5
 
 
 class Path(enum.IntEnum):
@@ -84,6 +86,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.awq_status_string.restype = ctypes.c_char_p
         lib.awq_last_device_status.argtypes = [_P]
         lib.awq_last_device_status.restype = _INT
+        lib.awq_linear_forward_decode_noalloc.argtypes = fwd_args
+        lib.awq_linear_forward_decode_noalloc.restype = _INT
         lib.awq_shutdown.argtypes = []
         lib.awq_shutdown.restype = None
         _lib = lib
@@ -125,3 +129,11 @@ def awq_last_device_status(stream) -> int:
 
 def awq_shutdown() -> None:
     load_library().awq_shutdown()
+
+
+def awq_linear_forward_decode_noalloc(x, qweight, qzeros, scales, bias, y, M, K, N, group_size,
+                                      stream) -> int:
+    """The decode forward with library-resident scratch: never allocates
+    device memory (see include/awq_gb300.h for who needs this and its limits)."""
+    return load_library().awq_linear_forward_decode_noalloc(x, qweight, qzeros, scales, bias, y,
+                                                            M, K, N, group_size, stream)

@@ -164,6 +164,8 @@ const char *awq_status_string(awq_status_t status)
     case AWQ_ERR_MISALIGNED: return "AWQ_ERR_MISALIGNED: a base pointer is not 16-byte aligned";
     case AWQ_ERR_CUDA: return "AWQ_ERR_CUDA: a CUDA call or kernel launch failed";
     case AWQ_ERR_TIMEOUT: return "AWQ_ERR_TIMEOUT: a kernel's bounded wait ran out";
+    case AWQ_ERR_TOO_LARGE:
+        return "AWQ_ERR_TOO_LARGE: shape exceeds the fixed scratch of the allocation-free entry point";
     default: return "AWQ: unknown status";
     }
 }

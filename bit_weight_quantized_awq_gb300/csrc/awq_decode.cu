@@ -582,3 +582,135 @@ cudaError_t launch_decode(const Problem &p, cudaStream_t stream)
 }
 
 } // namespace awq
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point: the decode kernel above, with its split-K
+// scratch taken from a fixed array compiled into this library instead of
+// memory the library allocates. The page has no counterpart of this call.
+// ---------------------------------------------------------------------------
+
+#include "../../include/awq_gb300.h"
+
+namespace awq {
+namespace {
+
+constexpr int kNoAllocMaxCtas = 160;    // grid cap: partial slots for 160 CTAs
+constexpr int kNoAllocMaxTiles = 8192;  // 256-column tiles: N up to 2,097,152
+constexpr size_t kNoAllocPartialWords = (size_t)2 * kNoAllocMaxCtas * kPartialFloats;
+constexpr size_t kNoAllocWords = kNoAllocPartialWords + (size_t)2 * kNoAllocMaxTiles;
+
+// fp32 partials (2 slots per CTA) followed by the arrival and departure
+// counters of every tile: 5,242,880 + 65,536 bytes on every GPU that loads
+// this library, for as long as the library stays loaded.
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocWords];
+
+// Device address of g_noalloc_scratch on the current device. Host code only
+// holds a stand-in for the symbol, so the address is looked up once per
+// device (with that device current) and cached.
+cudaError_t noalloc_scratch_address(uint32_t **out)
+{
+    static std::mutex mu;
+    static std::map<int, uint32_t *> addr;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = addr.find(dev);
+    if (it != addr.end()) {
+        *out = it->second;
+        return cudaSuccess;
+    }
+    uint32_t *ptr = nullptr;
+    e = cudaGetSymbolAddress(reinterpret_cast<void **>(&ptr), g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = ptr;
+    *out = ptr;
+    return cudaSuccess;
+}
+
+template <int MT>
+cudaError_t launch_decode_noalloc_t(const Problem &pr, cudaStream_t stream, uint32_t *scratch)
+{
+    const LaunchInfo li = launch_info<MT>();
+    if (li.err != cudaSuccess) return li.err;
+
+    const int M = (int)pr.M, K = (int)pr.K, N = (int)pr.N, g = (int)pr.g;
+    const int tiles = (N + kTileCols - 1) / kTileCols;
+    const int kiters = (K + kStageRows - 1) / kStageRows;
+    const int64_t total = (int64_t)tiles * kiters;
+    const int ctas = (int)std::min<int64_t>(std::min<int64_t>(total, (int64_t)li.occ * li.sms),
+                                            kNoAllocMaxCtas);
+    const int R = group_rows_per_stage(g);
+    const int mpad = 8 * MT;
+
+    CUtensorMap tw, tx, ts, tz;
+    bool ok = make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_INT32, pr.qweight, N / 8, K, (uint64_t)N / 2,
+                          kTileWords, kStageRows, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.x, K, M, (uint64_t)K * 2,
+                          kStageRows, mpad, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.scales, N, pr.G, (uint64_t)N * 2,
+                          kTileCols, R, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              make_map_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_INT32, pr.qzeros, N / 8, pr.G, (uint64_t)N / 2,
+                          kTileWords, R, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!ok) return cudaErrorInvalidValue;
+
+    DecodeParams p{};
+    p.bias = static_cast<const __half *>(pr.bias);
+    p.y = static_cast<__half *>(pr.y);
+    p.partials = reinterpret_cast<float *>(scratch);
+    p.arrive = scratch + kNoAllocPartialWords;
+    p.depart = p.arrive + tiles;
+    p.status = device_status_word();
+    p.M = M; p.K = K; p.N = N; p.g = g;
+    p.tiles = tiles; p.kiters = kiters; p.total = (int)total; p.ctas = ctas;
+    p.stage_tx = (uint32_t)(kWBytes + mpad * 128 + R * (kTileCols * 2) + R * (kTileWords * 4));
+
+    // the array keeps whatever the previous call left: the counters must
+    // start at zero (the partial slots are always written before being read)
+    cudaError_t e = cudaMemsetAsync(p.arrive, 0, sizeof(uint32_t) * 2 * (size_t)tiles, stream);
+    if (e != cudaSuccess) return e;
+
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_kernel<MT>, tw, tx, ts, tz, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+bool aligned16_ptr(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+} // namespace
+} // namespace awq
+
+extern "C" awq_status_t awq_linear_forward_decode_noalloc(
+    const void *x, const int32_t *qweight, const int32_t *qzeros, const void *scales,
+    const void *bias, void *y, int64_t M, int64_t K, int64_t N, int64_t group_size,
+    awq_stream_t stream)
+{
+    if (M < 0 || K <= 0 || N <= 0 || N % 8 != 0 || group_size == 0 || group_size < -1)
+        return AWQ_ERR_INVALID_ARG;
+    const int64_t g = (group_size == -1) ? K : group_size;
+    if (K % g != 0) return AWQ_ERR_INVALID_ARG;
+    if (M == 0) return AWQ_OK;
+    if (!x || !qweight || !qzeros || !scales || !y) return AWQ_ERR_INVALID_ARG;
+    if (!awq::aligned16_ptr(x) || !awq::aligned16_ptr(qweight) || !awq::aligned16_ptr(qzeros) ||
+        !awq::aligned16_ptr(scales) || !awq::aligned16_ptr(y) || (bias && !awq::aligned16_ptr(bias)))
+        return AWQ_ERR_MISALIGNED;
+    if (!awq::decode_supported(M, K, N, g)) return AWQ_ERR_INVALID_ARG;
+    if ((N + awq::kTileCols - 1) / awq::kTileCols > awq::kNoAllocMaxTiles) return AWQ_ERR_TOO_LARGE;
+    uint32_t *scratch = nullptr;
+    if (awq::noalloc_scratch_address(&scratch) != cudaSuccess) return AWQ_ERR_CUDA;
+    awq::Problem p{x, qweight, qzeros, scales, bias, y, M, K, N, g, K / g};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = (M <= 8) ? awq::launch_decode_noalloc_t<1>(p, s, scratch)
+                                   : awq::launch_decode_noalloc_t<2>(p, s, scratch);
+    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+}

@@ -61,7 +61,9 @@ typedef enum {
     AWQ_ERR_INVALID_ARG = 1, /* a shape rule of the WQLinear page, a NULL required pointer, M < 0 */
     AWQ_ERR_MISALIGNED = 2,  /* a base pointer is not 16-byte aligned */
     AWQ_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed */
-    AWQ_ERR_TIMEOUT = 4      /* a kernel's bounded wait ran out (device status only) */
+    AWQ_ERR_TIMEOUT = 4,     /* a kernel's bounded wait ran out (device status only) */
+    AWQ_ERR_TOO_LARGE = 5    /* the shape needs more than the fixed scratch of
+                                awq_linear_forward_decode_noalloc */
 } awq_status_t;
 
 /* Which kernel family serves a forward call. */
@@ -129,6 +131,43 @@ int awq_select_path(int64_t M, int64_t K, int64_t N, int64_t group_size);
 awq_status_t awq_dequant(const int32_t *qweight, const int32_t *qzeros,
                          const void *scales, void *W, int64_t K, int64_t N,
                          int64_t group_size, awq_stream_t stream);
+
+/*
+ * awq_linear_forward_decode_noalloc -- the same forward as awq_linear_forward,
+ * computed by the same decode kernel, for callers that must not have device
+ * memory allocated on their behalf. (The page has no counterpart of this
+ * call: it exists for how the library is embedded, not for the method.)
+ *
+ * Who needs it: a serving process that plans all of its device memory up
+ * front and may not allocate on the request path (a cudaMalloc there can
+ * stall the device and fragment memory that was budgeted to the last byte),
+ * and frameworks whose own caching allocator owns the GPU, where a hidden
+ * allocation is not accounted for and can fail once the framework has
+ * reserved nearly all of HBM. awq_linear_forward allocates a split-K scratch
+ * area on first use; this call never allocates. Its scratch is one array
+ * compiled into the library (5,308,416 bytes on every GPU that loads the
+ * library, held until the process exits).
+ *
+ * Arguments, layouts and result: as awq_linear_forward. It serves only the
+ * shapes the decode kernel takes (1 <= M <= 16, K % 16 == 0, N % 32 == 0,
+ * group_size % 16 == 0 after the -1 rule; else AWQ_ERR_INVALID_ARG) and at
+ * most 8192 column tiles of 256 (N <= 2,097,152; else AWQ_ERR_TOO_LARGE,
+ * returned before anything is enqueued). It uses at most 160 CTAs.
+ *
+ * The first call on a device looks up the array's device address and sets
+ * the kernel's launch attributes for that device; make that first call
+ * before any stream capture. Every call shares the one array and finds it as
+ * the previous call left it: each call clears the counters it needs
+ * (cudaMemsetAsync on `stream`), so calls ordered on the GPU are safe, and
+ * calls that overlap on the GPU (different streams, no ordering) race and
+ * give wrong results. No cudaMalloc, cudaFree or allocating library routine
+ * is called.
+ */
+awq_status_t awq_linear_forward_decode_noalloc(const void *x, const int32_t *qweight,
+                                               const int32_t *qzeros, const void *scales,
+                                               const void *bias, void *y, int64_t M,
+                                               int64_t K, int64_t N, int64_t group_size,
+                                               awq_stream_t stream);
 
 /* Static description of a status code. Never NULL. */
 const char *awq_status_string(awq_status_t status);
