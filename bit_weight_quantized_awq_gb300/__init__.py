@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401
     Path,
     Status,
     awq_dequant,
+    awq_gemm_f16,
     awq_last_device_status,
     awq_linear_forward,
     awq_linear_forward_decode_noalloc,

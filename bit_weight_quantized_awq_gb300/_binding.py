@@ -26,6 +26,7 @@ EXPORTED = (
     "awq_last_device_status",
     "awq_shutdown",
     "awq_linear_forward_decode_noalloc",
+    "awq_gemm_f16",
 )
 
 
@@ -88,6 +89,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.awq_last_device_status.restype = _INT
         lib.awq_linear_forward_decode_noalloc.argtypes = fwd_args
         lib.awq_linear_forward_decode_noalloc.restype = _INT
+        lib.awq_gemm_f16.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P]
+        lib.awq_gemm_f16.restype = _INT
         lib.awq_shutdown.argtypes = []
         lib.awq_shutdown.restype = None
         _lib = lib
@@ -117,6 +120,10 @@ def awq_select_path(M, K, N, group_size) -> int:
 
 def awq_dequant(qweight, qzeros, scales, W, K, N, group_size, stream) -> int:
     return load_library().awq_dequant(qweight, qzeros, scales, W, K, N, group_size, stream)
+
+
+def awq_gemm_f16(x, W, bias, y, M, K, N, stream) -> int:
+    return load_library().awq_gemm_f16(x, W, bias, y, M, K, N, stream)
 
 
 def awq_status_string(status) -> str:

@@ -240,6 +240,20 @@ awq_status_t awq_dequant(const int32_t *qweight, const int32_t *qzeros, const vo
     return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
 }
 
+awq_status_t awq_gemm_f16(const void *x, const void *W, const void *bias, void *y, int64_t M,
+                          int64_t K, int64_t N, awq_stream_t stream)
+{
+    if (M < 0 || K <= 0 || N <= 0) return AWQ_ERR_INVALID_ARG;
+    if (!awq::prefill_supported(M > 0 ? M : 1, K, N, 16)) return AWQ_ERR_INVALID_ARG;
+    if (M == 0) return AWQ_OK;
+    if (!x || !W || !y) return AWQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (bias && !aligned16(bias)))
+        return AWQ_ERR_MISALIGNED;
+    Problem p{x, nullptr, nullptr, nullptr, bias, y, M, K, N, K, 1};
+    cudaError_t e = awq::launch_gemm_f16(p, W, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+}
+
 awq_status_t awq_last_device_status(awq_stream_t stream)
 {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -52,4 +52,8 @@ cudaError_t launch_decode(const Problem &p, cudaStream_t stream);
 bool prefill_supported(int64_t M, int64_t K, int64_t N, int64_t g);
 cudaError_t launch_prefill(const Problem &p, cudaStream_t stream);
 
+// The prefill kernel's tensor-core pipeline on an already dequantised fp16
+// W [K, N] (no dequant stage): y = x . W + bias. Same shape rules as prefill.
+cudaError_t launch_gemm_f16(const Problem &p, const void *w16, cudaStream_t stream);
+
 } // namespace awq

@@ -133,6 +133,19 @@ awq_status_t awq_dequant(const int32_t *qweight, const int32_t *qzeros,
                          int64_t group_size, awq_stream_t stream);
 
 /*
+ * awq_gemm_f16 -- y[M, N] = fp16_rn(x[M, K] . W[K, N] + bias[N]) for an
+ * already dequantised fp16 W (row-major [K, N], e.g. from awq_dequant), on the
+ * same tcgen05 tensor-core pipeline as the prefill path of awq_linear_forward
+ * but without its dequant stage. It checks that pipeline on its own (against
+ * a library GEMM) and serves callers that keep W in fp16.
+ *   x fp16 [M, K], W fp16 [K, N], bias fp16 [N] or NULL, y fp16 [M, N].
+ * Requires K % 16 == 0 and N % 32 == 0 (AWQ_ERR_INVALID_ARG otherwise);
+ * pointer and M rules as awq_linear_forward.
+ */
+awq_status_t awq_gemm_f16(const void *x, const void *W, const void *bias, void *y, int64_t M,
+                          int64_t K, int64_t N, awq_stream_t stream);
+
+/*
  * awq_linear_forward_decode_noalloc -- the same forward as awq_linear_forward,
  * computed by the same decode kernel, for callers that must not have device
  * memory allocated on their behalf. (The page has no counterpart of this

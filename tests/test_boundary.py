@@ -34,7 +34,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(awq_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(awq_[a-z_0-9]+)\s*\(", text)))
 
 
 def test_every_declared_function_is_exported(lib):
