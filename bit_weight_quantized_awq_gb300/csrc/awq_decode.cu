@@ -16,8 +16,9 @@
 //    scale and zero-point rows of the groups the stage touches -- into an
 //    8-stage ring guarded by mbarriers (full: TMA bytes landed; empty: the
 //    consumers released the slot).
-//  * Math: 8 consumer warps (two groups of four that take alternate stages;
-//    each warp owns 64 columns) dequantise in registers and run the
+//  * Math: 16 consumer warps (four k-groups, each taking one 16-row chunk of
+//    every stage; in a group each warp owns 64 columns) dequantise in
+//    registers and run the
 //    legacy-path tensor-core MMA m16n8k16 with W as the A operand (16 output
 //    columns x 16 k) and the activations as B (16 k x 8 tokens), fp32
 //    accumulators. Two k-adjacent weights of one column form one half2
@@ -52,7 +53,7 @@ constexpr int kTileCols = 256;   // output columns per tile
 constexpr int kStageRows = 64;   // k-rows per pipeline stage
 constexpr int kStages = 8;
 constexpr int kColWarps = 4;     // warps across a tile's columns, 8 words each
-constexpr int kKGroups = 2;      // consumer groups taking alternate stages
+constexpr int kKGroups = 4;      // consumer groups, one 16-row chunk of every stage each
 constexpr int kConsumerWarps = kColWarps * kKGroups;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
@@ -70,7 +71,7 @@ constexpr int kStageBytes = 14 * 1024;
 static_assert(kZOff + kZBytes <= kStageBytes, "stage layout overflows");
 static_assert(kStageBytes % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 constexpr int kRedOff = kStages * kStageBytes;
-constexpr int kRedBytes = kMaxTokens * kTileCols * 4;
+constexpr int kRedBytes = (kKGroups - 1) * kMaxTokens * kTileCols * 4;
 constexpr int kBarOff = kRedOff + kRedBytes;
 constexpr int kSmemBytes = kBarOff + 256 + 1024;   // barriers + flags + alignment slack
 
@@ -137,7 +138,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(ptx::smem_addr(full + s), 1);
-            ptx::mbar_init(ptx::smem_addr(empty + s), kColWarps);
+            ptx::mbar_init(ptx::smem_addr(empty + s), kConsumerWarps);
         }
         *abort_flag = 0;
         *duty_ok = 0;
@@ -182,16 +183,36 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     }
 
     // ------------------------------------------------------------------ consumers
-    const int kg = warp / kColWarps;   // which alternate-stage group
+    const int kg = warp / kColWarps;   // which 16-row chunk of every stage
     const int cw = warp % kColWarps;   // which 64-column quarter of the tile
     const int gq = lane >> 2;          // MMA groupID: output column pair / token
     const int tq = lane & 3;           // MMA thread-in-group: k pair / token pair
     const int word = cw * 8 + gq;      // packed word (8 columns) this thread owns
-    const int ct = cw * 32 + lane;     // thread index within a group
+    const int ct = cw * 32 + lane;     // thread index within a k-group
+
+    // per-thread byte offsets inside a stage (the 128-byte swizzle phase of
+    // rows r0 and r0 + 8 is the same; so is that of r0 + 1 and r0 + 9)
+    const uint32_t wchunk = (uint32_t)(word >> 2);
+    const uint32_t inw = (uint32_t)(word & 3) * 4;
+    const int r0 = 16 * kg + 2 * tq;
+    const uint32_t offA = (uint32_t)r0 * 128 + ((wchunk ^ (uint32_t)(r0 & 7)) << 4) + inw;
+    const uint32_t offB = (uint32_t)(r0 + 1) * 128 + ((wchunk ^ (uint32_t)((r0 + 1) & 7)) << 4) + inw;
+    uint32_t xoff[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        const uint32_t xr = (uint32_t)(8 * mt + gq);
+        xoff[mt][0] = kXOff + xr * 128 + ((((uint32_t)(2 * kg)) ^ (xr & 7)) << 4) + 4 * tq;
+        xoff[mt][1] = kXOff + xr * 128 + ((((uint32_t)(2 * kg + 1)) ^ (xr & 7)) << 4) + 4 * tq;
+    }
+    const uint32_t soff = kSOff + (uint32_t)word * 16;
+    const uint32_t zoff = kZOff + (uint32_t)word * 4;
 
     float acc[4][MT][4];
     uint32_t S2[8], Zlo[4], Zhi[4];
-    int cur_group = -1;
+    int loaded_grp = -1;
+    // group index and offset inside the group of the stage's first row (st_)
+    // and of this warp's chunk (kc_), advanced by 64 rows per stage
+    int st_grp = 0, st_rem = 0, kc_grp = 0, kc_rem = 0;
     int seg_kb0 = 0;
     int duty_tiles[2] = {-1, -1};
     const int first_tile = begin / p.kiters;
@@ -200,111 +221,105 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         const int it = begin + i;
         const int tile = it / p.kiters;
         const int kb = it - tile * p.kiters;
+        const int k0 = kb * kStageRows;
         if (i == 0 || kb == 0) {
             seg_kb0 = kb;
-            cur_group = -1;
+            loaded_grp = -1;
+            st_grp = k0 / p.g;
+            st_rem = k0 - st_grp * p.g;
+            kc_grp = (k0 + 16 * kg) / p.g;
+            kc_rem = k0 + 16 * kg - kc_grp * p.g;
 #pragma unroll
             for (int b = 0; b < 4; ++b)
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) acc[b][mt][e] = 0.f;
+        } else {
+            st_rem += kStageRows;
+            while (st_rem >= p.g) { st_rem -= p.g; ++st_grp; }
+            kc_rem += kStageRows;
+            while (kc_rem >= p.g) { kc_rem -= p.g; ++kc_grp; }
         }
-        if ((i & 1) == kg) {
-            const int s = i % kStages;
-            // every lane waits (each needs the acquire); the MMA below is
-            // warp-wide, so the outcome is made uniform across the warp
-            const bool ok = __all_sync(0xffffffffu,
-                                       ptx::mbar_wait_bounded(ptx::smem_addr(full + s), (i / kStages) & 1,
-                                                              abort_flag, p.status));
-            if (ok) {
-                const uint32_t wbase = ptx::smem_addr(smem + s * kStageBytes);
-                const uint32_t xbase = wbase + kXOff;
-                const uint32_t sbase = wbase + kSOff;
-                const uint32_t zbase = wbase + kZOff;
-                const int k0 = kb * kStageRows;
-                const int grp0 = k0 / p.g;
+        const int s = i % kStages;
+        // every lane waits (each needs the acquire); the MMA below is
+        // warp-wide, so the outcome is made uniform across the warp
+        const bool ok = __all_sync(0xffffffffu,
+                                   ptx::mbar_wait_bounded(ptx::smem_addr(full + s), (i / kStages) & 1,
+                                                          abort_flag, p.status));
+        if (ok && k0 + 16 * kg < p.K) {
+            const uint32_t stb = ptx::smem_addr(smem + s * kStageBytes);
+            if (kc_grp != loaded_grp) {
+                loaded_grp = kc_grp;
+                const uint32_t r = (uint32_t)(kc_grp - st_grp);
+                uint4 sv;
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(sv.x), "=r"(sv.y), "=r"(sv.z), "=r"(sv.w)
+                             : "r"(stb + soff + r * (kTileCols * 2)));
+                const uint32_t zw = lds32(stb + zoff + r * (kTileWords * 4));
+                const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    const int kc = k0 + 16 * ch;
-                    if (kc >= p.K) break;
-                    const int grp = kc / p.g;
-                    if (grp != cur_group) {
-                        cur_group = grp;
-                        const int r = grp - grp0;
-                        uint4 sv;
-                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                     : "=r"(sv.x), "=r"(sv.y), "=r"(sv.z), "=r"(sv.w)
-                                     : "r"(sbase + r * (kTileCols * 2) + word * 16));
-                        const uint32_t zw = lds32(zbase + r * (kTileWords * 4) + word * 4);
-                        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+                for (int h = 0; h < 4; ++h) {
+                    S2[2 * h] = __byte_perm(sw[h], sw[h], 0x1010);
+                    S2[2 * h + 1] = __byte_perm(sw[h], sw[h], 0x3232);
+                }
 #pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            S2[2 * h] = __byte_perm(sw[h], sw[h], 0x1010);
-                            S2[2 * h + 1] = __byte_perm(sw[h], sw[h], 0x3232);
-                        }
-#pragma unroll
-                        for (int b = 0; b < 4; ++b) {
-                            const uint32_t t = __byte_perm(zw, zw, b | ((4 + b) << 8));
-                            Zlo[b] = (t & 0x000F000Fu) | 0x64006400u;
-                            Zhi[b] = (t & 0x00F000F0u) | 0x54005400u;
-                        }
-                    }
-                    // packed words of rows 16ch + 2tq (+1, +8, +9), 128-byte swizzle
-                    const int r0 = 16 * ch + 2 * tq;
-                    const uint32_t chunk = (uint32_t)(word >> 2);
-                    const uint32_t inw = (uint32_t)(word & 3) * 4;
-                    auto waddr = [&](int r) {
-                        return wbase + r * 128 + ((chunk ^ (uint32_t)(r & 7)) << 4) + inw;
-                    };
-                    const uint32_t v0 = lds32(waddr(r0));
-                    const uint32_t v1 = lds32(waddr(r0 + 1));
-                    const uint32_t v8 = lds32(waddr(r0 + 8));
-                    const uint32_t v9 = lds32(waddr(r0 + 9));
-                    uint32_t bf[MT][2];
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        const int xr = 8 * mt + gq;
-                        bf[mt][0] = lds32(xbase + xr * 128 + (((uint32_t)(2 * ch) ^ (uint32_t)(xr & 7)) << 4) + 4 * tq);
-                        bf[mt][1] = lds32(xbase + xr * 128 + (((uint32_t)(2 * ch + 1) ^ (uint32_t)(xr & 7)) << 4) + 4 * tq);
-                    }
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        const uint32_t sel = (uint32_t)(b | ((4 + b) << 8));
-                        const uint32_t t01 = __byte_perm(v0, v1, sel);
-                        const uint32_t t89 = __byte_perm(v8, v9, sel);
-                        uint32_t a[4];
-                        a[0] = hmul2_u(hsub2_u((t01 & 0x000F000Fu) | 0x64006400u, Zlo[b]), S2[2 * b]);
-                        a[1] = hmul2_u(hsub2_u((t01 & 0x00F000F0u) | 0x54005400u, Zhi[b]), S2[2 * b + 1]);
-                        a[2] = hmul2_u(hsub2_u((t89 & 0x000F000Fu) | 0x64006400u, Zlo[b]), S2[2 * b]);
-                        a[3] = hmul2_u(hsub2_u((t89 & 0x00F000F0u) | 0x54005400u, Zhi[b]), S2[2 * b + 1]);
-#pragma unroll
-                        for (int mt = 0; mt < MT; ++mt) ptx::mma_16816(acc[b][mt], a, bf[mt][0], bf[mt][1]);
-                    }
+                for (int b = 0; b < 4; ++b) {
+                    const uint32_t t = __byte_perm(zw, zw, b | ((4 + b) << 8));
+                    Zlo[b] = (t & 0x000F000Fu) | 0x64006400u;
+                    Zhi[b] = (t & 0x00F000F0u) | 0x54005400u;
                 }
             }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(empty + s));
+            const uint32_t v0 = lds32(stb + offA);
+            const uint32_t v1 = lds32(stb + offB);
+            const uint32_t v8 = lds32(stb + offA + 1024);
+            const uint32_t v9 = lds32(stb + offB + 1024);
+            uint32_t bf[MT][2];
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                bf[mt][0] = lds32(stb + xoff[mt][0]);
+                bf[mt][1] = lds32(stb + xoff[mt][1]);
+            }
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const uint32_t sel = (uint32_t)(b | ((4 + b) << 8));
+                const uint32_t t01 = __byte_perm(v0, v1, sel);
+                const uint32_t t89 = __byte_perm(v8, v9, sel);
+                uint32_t a[4];
+                a[0] = hmul2_u(hsub2_u((t01 & 0x000F000Fu) | 0x64006400u, Zlo[b]), S2[2 * b]);
+                a[1] = hmul2_u(hsub2_u((t01 & 0x00F000F0u) | 0x54005400u, Zhi[b]), S2[2 * b + 1]);
+                a[2] = hmul2_u(hsub2_u((t89 & 0x000F000Fu) | 0x64006400u, Zlo[b]), S2[2 * b]);
+                a[3] = hmul2_u(hsub2_u((t89 & 0x00F000F0u) | 0x54005400u, Zhi[b]), S2[2 * b + 1]);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) ptx::mma_16816(acc[b][mt], a, bf[mt][0], bf[mt][1]);
+            }
         }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(empty + s));
 
         if (i == n_iters - 1 || kb == p.kiters - 1) {
-            // ---- segment end: fold the second group's sums into the first's
-            if (kg == 1) {
+            // ---- segment end: fold k-groups 1..3 into k-group 0, in that order
+            if (kg > 0) {
+                float *dst = red + (kg - 1) * (MT * 16 * 128);
 #pragma unroll
                 for (int b = 0; b < 4; ++b)
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) red[(b * MT + mt) * 512 + e * 128 + ct] = acc[b][mt][e];
+                        for (int e = 0; e < 4; ++e) dst[((b * MT + mt) * 4 + e) * 128 + ct] = acc[b][mt][e];
             }
             ptx::named_barrier(1, kConsumerThreads);
             if (kg == 0) {
+#pragma unroll 1
+                for (int src = 0; src < kKGroups - 1; ++src) {
+                    const float *from = red + src * (MT * 16 * 128);
 #pragma unroll
-                for (int b = 0; b < 4; ++b)
+                    for (int b = 0; b < 4; ++b)
 #pragma unroll
-                    for (int mt = 0; mt < MT; ++mt)
+                        for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) acc[b][mt][e] += red[(b * MT + mt) * 512 + e * 128 + ct];
+                            for (int e = 0; e < 4; ++e) acc[b][mt][e] += from[((b * MT + mt) * 4 + e) * 128 + ct];
+                }
             }
             ptx::named_barrier(1, kConsumerThreads);
 
@@ -376,6 +391,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         const int cf = cta_of(t * p.kiters, p.total, p.ctas);
         const int cl = cta_of((t + 1) * p.kiters - 1, p.total, p.ctas);
         const int n = cl - cf + 1;
+        // every contributor after the first starts inside tile t, so its
+        // partial of t is in its first slot; the first one may have started
+        // in an earlier tile
+        const int which_cf = (range_begin(cf, p.total, p.ctas) / p.kiters == t) ? 0 : 1;
         if (ctid == 0) {
             bool ok = !*abort_flag;
             if (ok) {
@@ -387,7 +406,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                         atomicOr(p.status, kStatusTimeout);
                         break;
                     }
-                    __nanosleep(64);
+                    __nanosleep(32);
                 }
             }
             *duty_ok = ok ? 1 : 0;
@@ -403,16 +422,30 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 const int w = u - m * kTileWords;
                 const int col0 = t * kTileCols + w * 8;
                 if (col0 >= p.N) continue;
+                const int64_t inner = (int64_t)m * kTileCols + w * 8;
                 float s8[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) s8[j] = 0.f;
-                for (int cc = cf; cc <= cl; ++cc) {
-                    const int which = (t == range_begin(cc, p.total, p.ctas) / p.kiters) ? 0 : 1;
-                    const float4 *src = reinterpret_cast<const float4 *>(
-                        p.partials + (int64_t)(2 * cc + which) * kPartialFloats + m * kTileCols + w * 8);
-                    const float4 lo = __ldcg(src), hi = __ldcg(src + 1);
-                    s8[0] += lo.x; s8[1] += lo.y; s8[2] += lo.z; s8[3] += lo.w;
-                    s8[4] += hi.x; s8[5] += hi.y; s8[6] += hi.z; s8[7] += hi.w;
+                // contributors in ascending order; loads issued 4 at a time
+                for (int cc = cf; cc <= cl; cc += 4) {
+                    float4 lo[4], hi[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (cc + j <= cl) {
+                            const int slot = 2 * (cc + j) + ((cc + j) == cf ? which_cf : 0);
+                            const float4 *src = reinterpret_cast<const float4 *>(
+                                p.partials + (int64_t)slot * kPartialFloats + inner);
+                            lo[j] = __ldcg(src);
+                            hi[j] = __ldcg(src + 1);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (cc + j <= cl) {
+                            s8[0] += lo[j].x; s8[1] += lo[j].y; s8[2] += lo[j].z; s8[3] += lo[j].w;
+                            s8[4] += hi[j].x; s8[5] += hi[j].y; s8[6] += hi[j].z; s8[7] += hi[j].w;
+                        }
+                    }
                 }
                 __align__(16) __half out[8];
                 if (p.bias) {
