@@ -259,8 +259,11 @@ def run_native(args, problems, device):
     except Exception:
         use_events = False
         graphs = [capture_step(items, path, stream, False) for items in sets]
-    for i in range(args.warmup):
-        graphs[i % len(graphs)][0].replay()
+    # CUDAGraph.replay() launches on the current stream: make it `stream`,
+    # the stream the timing events are recorded on
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % len(graphs)][0].replay()
     torch.cuda.synchronize(device)
 
     ws, rank, local = dist_env()
@@ -269,10 +272,11 @@ def run_native(args, problems, device):
         barrier(device)
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        for i in range(args.steps):
-            graphs[i % len(graphs)][0].replay()
-        end.record(stream)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for i in range(args.steps):
+                graphs[i % len(graphs)][0].replay()
+            end.record(stream)
         barrier(device)
     elapsed = start.elapsed_time(end) / 1e3
     clocks = clk.summary()
@@ -442,13 +446,16 @@ def run_sweep(args, device, peaks):
                 graph = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(graph, stream=stream):
                     for r in range(reps):
-                        launch(sets[r % len(sets)][0], path, handle)
-                graph.replay()
-                torch.cuda.synchronize(device)
+                        st = launch(sets[r % len(sets)][0], path, handle)
+                        if st != 0:
+                            raise RuntimeError(f"status {st} capturing {prob} on {path.name}")
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                graph.replay()
-                e1.record(stream)
+                with torch.cuda.stream(stream):
+                    graph.replay()
+                    stream.synchronize()
+                    e0.record(stream)
+                    graph.replay()
+                    e1.record(stream)
                 torch.cuda.synchronize(device)
                 t = e0.elapsed_time(e1) / 1e3 / reps
                 row = {"workload": wl, "M": M, "K": K, "N": N, "g": g, "bias": bias,

@@ -398,9 +398,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         if (ctid == 0) {
             bool ok = !*abort_flag;
             if (ok) {
-                const uint64_t t0 = ptx::globaltimer();
+                const long long t0 = clock64();
                 while (ptx::ld_acquire_gpu(p.arrive + t) < (unsigned)n) {
-                    if (*abort_flag || ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+                    if (*abort_flag || clock64() - t0 > ptx::kWaitLimitCycles) {
                         ok = false;
                         *abort_flag = 1;
                         atomicOr(p.status, kStatusTimeout);

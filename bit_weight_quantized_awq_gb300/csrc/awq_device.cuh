@@ -96,9 +96,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Device-side wait limit: a wait that has not completed after this long
-// records AWQ_ERR_TIMEOUT in the status word and gives up.
-constexpr uint64_t kWaitLimitNs = 2000000000ull; // 2 s
+// Device-side wait limit: a wait that has not completed after this many SM
+// clock cycles (about 2 s at 2 GHz, longer at lower clocks) records
+// AWQ_ERR_TIMEOUT in the status word and gives up. The limit is kept with the
+// SM-local cycle counter: reading %globaltimer costs far more than a poll.
+constexpr long long kWaitLimitCycles = 4000000000ll;
 
 // Bounded wait on an mbarrier phase. Returns false if the wait gave up,
 // either because its own limit ran out or because another thread of the CTA
@@ -106,14 +108,16 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull; // 2 s
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int *abort, unsigned int *status) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    while (true) {
+    const long long t0 = clock64();
+    for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (abort && *abort) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
-            if (abort) *abort = 1;
-            if (status) atomicOr(status, 1u);
-            return false;
+        if ((n & 255u) == 0) {
+            if (abort && *abort) return false;
+            if (clock64() - t0 > kWaitLimitCycles) {
+                if (abort) *abort = 1;
+                if (status) atomicOr(status, 1u);
+                return false;
+            }
         }
     }
 }
