@@ -8,24 +8,26 @@
 // (0.52 bytes per weight at g = 128). The kernel is built around that:
 //
 //  * Work: the K x N weight matrix is cut into tiles of 256 columns (one
-//    128-byte row of packed words) and stage blocks of 64 k-rows. The
-//    (tile, block) iterations, tile-major, are split evenly between the CTAs
-//    (one per SM): each CTA streams a contiguous run of them ("stream-K").
-//  * Loads: one producer warp issues 2-D TMA boxes per stage -- 64 x 128 B of
-//    qweight (128-byte swizzle), the 64 x Mpad activation slice, and the
-//    scale and zero-point rows of the groups the stage touches -- into an
-//    8-stage ring guarded by mbarriers (full: TMA bytes landed; empty: the
-//    consumers released the slot).
-//  * Math: 16 consumer warps (four k-groups, each taking one 16-row chunk of
-//    every stage; in a group each warp owns 64 columns) dequantise in
-//    registers and run the
-//    legacy-path tensor-core MMA m16n8k16 with W as the A operand (16 output
-//    columns x 16 k) and the activations as B (16 k x 8 tokens), fp32
-//    accumulators. Two k-adjacent weights of one column form one half2
-//    operand register: a byte permute brings byte b of rows k and k+1
-//    together, one LOP3 masks a nibble into the fraction of 1024.0 or 64.0,
-//    an exact half2 subtract removes the zero point and one half2 multiply
-//    (round to nearest) applies the scale -- exactly fp16_rn((q - z) s).
+//    128-byte row of packed words) and stages of 256 k-rows. The (tile,
+//    stage) iterations, tile-major, are split evenly between the CTAs (one
+//    per SM): each CTA streams a contiguous run of them ("stream-K").
+//  * Loads: one producer warp issues four TMA boxes per stage -- 256 x 128 B
+//    of qweight (32 KB, 128-byte swizzle), the 256 x Mpad activation slice
+//    (one 3-D box), and the scale and zero-point rows of the groups the stage
+//    touches -- into a 4-stage ring guarded by mbarriers (full: bytes landed;
+//    empty: the consumers released the slot). Issuing a TMA instruction costs
+//    the producer on the order of a hundred cycles, so each one moves as many
+//    bytes as the box limits allow.
+//  * Math: 8 consumer warps: two k-groups (group kg takes rows 128 kg ..
+//    128 kg + 127 of every stage, eight 16-row chunks) of four warps (each
+//    owns 64 columns). Each warp dequantises in registers and runs the legacy-path
+//    tensor-core MMA m16n8k16 with W as the A operand (16 output columns x 16
+//    k) and the activations as B (16 k x 8 tokens), fp32 accumulators. Two
+//    k-adjacent weights of one column form one half2 operand register: a byte
+//    permute brings byte b of rows k and k+1 together, one LOP3 masks a nibble
+//    into the fraction of 1024.0 or 64.0, an exact half2 subtract removes the
+//    zero point and one half2 multiply (round to nearest) applies the scale --
+//    exactly fp16_rn((q - z) s).
 //  * Reduction: a tile split between CTAs is summed by its contributors
 //    together at the end of the kernel: each writes its fp32 partial to
 //    scratch and counts itself in; after its own stream is done it waits
@@ -33,8 +35,9 @@
 //    fixed contributor order, adding the bias and rounding once. The grid is
 //    launched cooperatively so that every CTA is resident.
 //
-// Requirements (else the generic kernel serves): 1 <= M <= 16, K % 16 == 0,
-// N % 32 == 0 (TMA row pitch), g % 16 == 0, base pointers 16-byte aligned.
+// Requirements (else another path serves): 1 <= M <= 16, K % 64 == 0,
+// N % 32 == 0 (TMA row pitch), g % 16 == 0 with at most 8 groups per 256-row
+// stage (g >= 32), base pointers 16-byte aligned.
 #include <algorithm>
 #include <map>
 #include <mutex>
@@ -50,30 +53,42 @@ namespace {
 
 constexpr int kTileWords = 32;   // packed words per tile row
 constexpr int kTileCols = 256;   // output columns per tile
-constexpr int kStageRows = 64;   // k-rows per pipeline stage
-constexpr int kStages = 8;
+constexpr int kStageRows = 256;  // k-rows per pipeline stage
+constexpr int kStages = 4;
+constexpr int kKBlocks = kStageRows / 64;   // 64-row blocks of a stage (activation layout)
 constexpr int kColWarps = 4;     // warps across a tile's columns, 8 words each
-constexpr int kKGroups = 4;      // consumer groups, one 16-row chunk of every stage each
-constexpr int kConsumerWarps = kColWarps * kKGroups;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+
+// Warp layout for KG consumer k-groups: k-group kg takes stage rows
+// kRowsPerWarp * kg .. + kRowsPerWarp - 1, split in 16-row chunks; each of its
+// kColWarps warps owns 64 columns. One producer warp follows the consumers.
+template <int KG>
+struct Layout {
+    static constexpr int kKGroups = KG;
+    static constexpr int kRowsPerWarp = kStageRows / KG;
+    static constexpr int kChunksPerWarp = kRowsPerWarp / 16;
+    static constexpr int kConsumerWarps = kColWarps * KG;
+    static constexpr int kConsumerThreads = kConsumerWarps * 32;
+    static constexpr int kThreads = kConsumerThreads + 32;
+};
 constexpr int kMaxTokens = 16;
-constexpr int kMaxGroupRows = 5; // group rows one 64-row stage can touch when g >= 16
+constexpr int kMaxGroupRows = 8; // group rows one stage may touch (g >= 32)
 
 constexpr int kWBytes = kStageRows * 128;
-constexpr int kXBytes = kMaxTokens * 128;
+constexpr int kXBytes = kMaxTokens * kStageRows * 2;
 constexpr int kSBytes = kMaxGroupRows * kTileCols * 2;
 constexpr int kZBytes = kMaxGroupRows * kTileWords * 4;
 constexpr int kXOff = kWBytes;
 constexpr int kSOff = kXOff + kXBytes;
 constexpr int kZOff = kSOff + kSBytes;
-constexpr int kStageBytes = 14 * 1024;
+constexpr int kStageBytes = 45 * 1024;
 static_assert(kZOff + kZBytes <= kStageBytes, "stage layout overflows");
-static_assert(kStageBytes % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(kStageBytes % 1024 == 0 && kXOff % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+constexpr int kFoldFloats = kMaxTokens * kTileCols;     // one k-group's sums
 constexpr int kRedOff = kStages * kStageBytes;
-constexpr int kRedBytes = (kKGroups - 1) * kMaxTokens * kTileCols * 4;
+constexpr int kRedBytes = 2 * kFoldFloats * 4;
 constexpr int kBarOff = kRedOff + kRedBytes;
 constexpr int kSmemBytes = kBarOff + 256 + 1024;   // barriers + flags + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 constexpr int kPartialFloats = kMaxTokens * kTileCols;  // one partial slot
 
@@ -88,12 +103,6 @@ struct DecodeParams {
     int tiles, kiters, total, ctas;
     uint32_t stage_tx;      // bytes one stage's TMA boxes deliver
 };
-
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
-}
 
 __device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
     __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
@@ -114,20 +123,46 @@ __device__ __forceinline__ int range_begin(int c, int total, int ctas) {
 }
 
 template <int MT>
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ void fold_store(float *dst, const float (&acc)[4][MT][4], int ct) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst[((b * MT + mt) * 4 + e) * 128 + ct] = acc[b][mt][e];
+}
+template <int MT>
+__device__ __forceinline__ void fold_add(const float *src, float (&acc)[4][MT][4], int ct) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[b][mt][e] += src[((b * MT + mt) * 4 + e) * 128 + ct];
+}
+
+template <int MT, int KG, bool kWholeGroups>
+__global__ void __launch_bounds__(Layout<KG>::kThreads, 1)
 decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
               const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
               const DecodeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // round up to 1024 bytes by offsetting the shared array itself, so that
+    // the compiler still knows every derived pointer is a shared address
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
     float *red = reinterpret_cast<float *>(smem + kRedOff);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kBarOff);
     uint64_t *empty = full + kStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStages);
     volatile int *duty_ok = abort_flag + 1;
+    volatile uint32_t *consts = reinterpret_cast<volatile uint32_t *>(abort_flag + 2);
 
+    using L = Layout<KG>;
+    constexpr int kConsumerWarps = L::kConsumerWarps;
+    constexpr int kConsumerThreads = L::kConsumerThreads;
+    constexpr int kChunksPerWarp = L::kChunksPerWarp;
+    constexpr int kRowsPerWarp = L::kRowsPerWarp;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int c = blockIdx.x;
@@ -142,6 +177,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         }
         *abort_flag = 0;
         *duty_ok = 0;
+        consts[0] = 0x64006400u;   // 1024.0 in both halves
+        consts[1] = 0x54005400u;   // 64.0 in both halves
         ptx::fence_mbar_init();
     }
     __syncthreads();
@@ -154,10 +191,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             ptx::prefetch_tmap(&tm_s);
             ptx::prefetch_tmap(&tm_z);
             int issued = 0;
+            int tile = begin / p.kiters;
+            int kb = begin - tile * p.kiters;
             for (int i = 0; i < n_iters; ++i) {
-                const int it = begin + i;
-                const int tile = it / p.kiters;
-                const int kb = it - tile * p.kiters;
                 const int s = i % kStages;
                 const uint32_t parity = ((i / kStages) & 1) ^ 1;
                 if (!ptx::mbar_wait_bounded(ptx::smem_addr(empty + s), parity, abort_flag, p.status))
@@ -165,12 +201,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 const uint32_t fb = ptx::smem_addr(full + s);
                 const uint32_t st = ptx::smem_addr(smem + s * kStageBytes);
                 const int k0 = kb * kStageRows;
+                const int grp0 = k0 / p.g;
                 ptx::mbar_arrive_expect_tx(fb, p.stage_tx);
                 ptx::tma_load_2d(st, &tm_w, fb, tile * kTileWords, k0);
-                ptx::tma_load_2d(st + kXOff, &tm_x, fb, k0, 0);
-                ptx::tma_load_2d(st + kSOff, &tm_s, fb, tile * kTileCols, k0 / p.g);
-                ptx::tma_load_2d(st + kZOff, &tm_z, fb, tile * kTileWords, k0 / p.g);
+                ptx::tma_load_3d(st + kXOff, &tm_x, fb, 0, k0 / 64, 0);
+                ptx::tma_load_2d(st + kSOff, &tm_s, fb, tile * kTileCols, grp0);
+                ptx::tma_load_2d(st + kZOff, &tm_z, fb, tile * kTileWords, grp0);
                 issued = i + 1;
+                if (++kb == p.kiters) { kb = 0; ++tile; }
             }
             if (*abort_flag) {
                 // let the copies already in flight land before the CTA exits
@@ -183,52 +221,83 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     }
 
     // ------------------------------------------------------------------ consumers
-    const int kg = warp / kColWarps;   // which 16-row chunk of every stage
+    const int kg = warp / kColWarps;   // rows kRowsPerWarp * kg .. of every stage
     const int cw = warp % kColWarps;   // which 64-column quarter of the tile
     const int gq = lane >> 2;          // MMA groupID: output column pair / token
     const int tq = lane & 3;           // MMA thread-in-group: k pair / token pair
     const int word = cw * 8 + gq;      // packed word (8 columns) this thread owns
     const int ct = cw * 32 + lane;     // thread index within a k-group
 
-    // per-thread byte offsets inside a stage (the 128-byte swizzle phase of
-    // rows r0 and r0 + 8 is the same; so is that of r0 + 1 and r0 + 9)
+    // Byte offsets inside a stage. Chunk j of this warp is stage rows
+    // R0 + 16 j .. +15 (R0 = kRowsPerWarp kg); rows 16ch + 2tq (+1) sit at a
+    // fixed 128-byte swizzle phase, rows +8 / +9 one 1024-byte atom further.
+    const int R0 = kRowsPerWarp * kg;
     const uint32_t wchunk = (uint32_t)(word >> 2);
     const uint32_t inw = (uint32_t)(word & 3) * 4;
-    const int r0 = 16 * kg + 2 * tq;
-    const uint32_t offA = (uint32_t)r0 * 128 + ((wchunk ^ (uint32_t)(r0 & 7)) << 4) + inw;
-    const uint32_t offB = (uint32_t)(r0 + 1) * 128 + ((wchunk ^ (uint32_t)((r0 + 1) & 7)) << 4) + inw;
-    uint32_t xoff[MT][2];
+    const uint32_t rA = (uint32_t)(2 * tq), rB = rA + 1;
+    const uint32_t offA = (uint32_t)R0 * 128 + rA * 128 + ((wchunk ^ rA) << 4) + inw;
+    const uint32_t offB = (uint32_t)R0 * 128 + rB * 128 + ((wchunk ^ rB) << 4) + inw;
+    // activation slice: [token m][64-row block][64 halves], 128-byte rows;
+    // chunk j of this warp is in block R0 / 64 + j / 4, 16-byte units
+    // 2 (j % 4) and 2 (j % 4) + 1. The 128-byte swizzle XORs bits 4..6 of the
+    // offset, which are zero in the row base, so the address of unit u is
+    // (row base | phase) ^ (u << 4).
+    constexpr int kBlocksPerWarp = (kChunksPerWarp + 3) / 4;
+    uint32_t xrow[MT][kBlocksPerWarp];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-        const uint32_t xr = (uint32_t)(8 * mt + gq);
-        xoff[mt][0] = kXOff + xr * 128 + ((((uint32_t)(2 * kg)) ^ (xr & 7)) << 4) + 4 * tq;
-        xoff[mt][1] = kXOff + xr * 128 + ((((uint32_t)(2 * kg + 1)) ^ (xr & 7)) << 4) + 4 * tq;
-    }
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int jb = 0; jb < kBlocksPerWarp; ++jb) {
+            const uint32_t r = (uint32_t)((8 * mt + gq) * kKBlocks + R0 / 64 + jb);
+            xrow[mt][jb] = (kXOff + r * 128 + 4 * tq) | ((r & 7) << 4);
+        }
     const uint32_t soff = kSOff + (uint32_t)word * 16;
     const uint32_t zoff = kZOff + (uint32_t)word * 4;
+    // the fp16 exponent patterns OR-ed into the nibbles, read from shared
+    // memory so that they stay in registers instead of being rebuilt before
+    // every use (a LOP3 takes only one immediate operand)
+    const uint32_t base_lo = consts[0];
+    const uint32_t base_hi = consts[1];
 
     float acc[4][MT][4];
     uint32_t S2[8], Zlo[4], Zhi[4];
     int loaded_grp = -1;
-    // group index and offset inside the group of the stage's first row (st_)
-    // and of this warp's chunk (kc_), advanced by 64 rows per stage
-    int st_grp = 0, st_rem = 0, kc_grp = 0, kc_rem = 0;
+    // group index and offset inside its group of the stage's first row (st_)
+    // and of this warp's first row (wg_)
+    int st_grp = 0, st_rem = 0, wg_grp = 0, wg_rem = 0;
     int seg_kb0 = 0;
     int duty_tiles[2] = {-1, -1};
     const int first_tile = begin / p.kiters;
+    int tile = first_tile;
+    int kb = begin - tile * p.kiters;
+
+    // loads this thread's 8 scales and zero points of group row r of a stage
+    auto load_group = [&](const uint8_t *stp, uint32_t r) {
+        const uint4 sv = *reinterpret_cast<const uint4 *>(stp + soff + r * (kTileCols * 2));
+        const uint32_t zw = *reinterpret_cast<const uint32_t *>(stp + zoff + r * (kTileWords * 4));
+        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            S2[2 * h] = __byte_perm(sw[h], sw[h], 0x1010);
+            S2[2 * h + 1] = __byte_perm(sw[h], sw[h], 0x3232);
+        }
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const uint32_t t = __byte_perm(zw, zw, b | ((4 + b) << 8));
+            Zlo[b] = (t & 0x000F000Fu) | base_lo;
+            Zhi[b] = (t & 0x00F000F0u) | base_hi;
+        }
+    };
 
     for (int i = 0; i < n_iters; ++i) {
-        const int it = begin + i;
-        const int tile = it / p.kiters;
-        const int kb = it - tile * p.kiters;
         const int k0 = kb * kStageRows;
         if (i == 0 || kb == 0) {
             seg_kb0 = kb;
             loaded_grp = -1;
             st_grp = k0 / p.g;
             st_rem = k0 - st_grp * p.g;
-            kc_grp = (k0 + 16 * kg) / p.g;
-            kc_rem = k0 + 16 * kg - kc_grp * p.g;
+            wg_grp = (k0 + R0) / p.g;
+            wg_rem = k0 + R0 - wg_grp * p.g;
 #pragma unroll
             for (int b = 0; b < 4; ++b)
 #pragma unroll
@@ -238,8 +307,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         } else {
             st_rem += kStageRows;
             while (st_rem >= p.g) { st_rem -= p.g; ++st_grp; }
-            kc_rem += kStageRows;
-            while (kc_rem >= p.g) { kc_rem -= p.g; ++kc_grp; }
+            wg_rem += kStageRows;
+            while (wg_rem >= p.g) { wg_rem -= p.g; ++wg_grp; }
         }
         const int s = i % kStages;
         // every lane waits (each needs the acquire); the MMA below is
@@ -247,80 +316,69 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         const bool ok = __all_sync(0xffffffffu,
                                    ptx::mbar_wait_bounded(ptx::smem_addr(full + s), (i / kStages) & 1,
                                                           abort_flag, p.status));
-        if (ok && k0 + 16 * kg < p.K) {
-            const uint32_t stb = ptx::smem_addr(smem + s * kStageBytes);
-            if (kc_grp != loaded_grp) {
-                loaded_grp = kc_grp;
-                const uint32_t r = (uint32_t)(kc_grp - st_grp);
-                uint4 sv;
-                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(sv.x), "=r"(sv.y), "=r"(sv.z), "=r"(sv.w)
-                             : "r"(stb + soff + r * (kTileCols * 2)));
-                const uint32_t zw = lds32(stb + zoff + r * (kTileWords * 4));
-                const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+        if (ok && k0 + R0 < p.K) {
+            const uint8_t *stp = smem + s * kStageBytes;
+            if (kWholeGroups) {
+                // g % kRowsPerWarp == 0: the warp's rows lie in one group
+                if (wg_grp != loaded_grp) {
+                    loaded_grp = wg_grp;
+                    load_group(stp, (uint32_t)(wg_grp - st_grp));
+                }
+            }
+            int grp = wg_grp, rem = wg_rem;
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    S2[2 * h] = __byte_perm(sw[h], sw[h], 0x1010);
-                    S2[2 * h + 1] = __byte_perm(sw[h], sw[h], 0x3232);
+            for (int j = 0; j < kChunksPerWarp; ++j) {
+                if (!kWholeGroups) {
+                    if (j > 0) {
+                        rem += 16;
+                        if (rem >= p.g) { rem -= p.g; ++grp; }
+                    }
+                    if (grp != loaded_grp) {
+                        loaded_grp = grp;
+                        load_group(stp, (uint32_t)(grp - st_grp));
+                    }
+                }
+                const uint8_t *wp = stp + j * (16 * 128);
+                const uint32_t v0 = *reinterpret_cast<const uint32_t *>(wp + offA);
+                const uint32_t v1 = *reinterpret_cast<const uint32_t *>(wp + offB);
+                const uint32_t v8 = *reinterpret_cast<const uint32_t *>(wp + offA + 1024);
+                const uint32_t v9 = *reinterpret_cast<const uint32_t *>(wp + offB + 1024);
+                uint32_t bf[MT][2];
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    bf[mt][0] = *reinterpret_cast<const uint32_t *>(stp + (xrow[mt][j / 4] ^ (uint32_t)((2 * (j % 4)) << 4)));
+                    bf[mt][1] = *reinterpret_cast<const uint32_t *>(stp + (xrow[mt][j / 4] ^ (uint32_t)((2 * (j % 4) + 1) << 4)));
                 }
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
-                    const uint32_t t = __byte_perm(zw, zw, b | ((4 + b) << 8));
-                    Zlo[b] = (t & 0x000F000Fu) | 0x64006400u;
-                    Zhi[b] = (t & 0x00F000F0u) | 0x54005400u;
+                    const uint32_t sel = (uint32_t)(b | ((4 + b) << 8));
+                    const uint32_t t01 = __byte_perm(v0, v1, sel);
+                    const uint32_t t89 = __byte_perm(v8, v9, sel);
+                    uint32_t a[4];
+                    a[0] = hmul2_u(hsub2_u((t01 & 0x000F000Fu) | base_lo, Zlo[b]), S2[2 * b]);
+                    a[1] = hmul2_u(hsub2_u((t01 & 0x00F000F0u) | base_hi, Zhi[b]), S2[2 * b + 1]);
+                    a[2] = hmul2_u(hsub2_u((t89 & 0x000F000Fu) | base_lo, Zlo[b]), S2[2 * b]);
+                    a[3] = hmul2_u(hsub2_u((t89 & 0x00F000F0u) | base_hi, Zhi[b]), S2[2 * b + 1]);
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) ptx::mma_16816(acc[b][mt], a, bf[mt][0], bf[mt][1]);
                 }
-            }
-            const uint32_t v0 = lds32(stb + offA);
-            const uint32_t v1 = lds32(stb + offB);
-            const uint32_t v8 = lds32(stb + offA + 1024);
-            const uint32_t v9 = lds32(stb + offB + 1024);
-            uint32_t bf[MT][2];
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                bf[mt][0] = lds32(stb + xoff[mt][0]);
-                bf[mt][1] = lds32(stb + xoff[mt][1]);
-            }
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const uint32_t sel = (uint32_t)(b | ((4 + b) << 8));
-                const uint32_t t01 = __byte_perm(v0, v1, sel);
-                const uint32_t t89 = __byte_perm(v8, v9, sel);
-                uint32_t a[4];
-                a[0] = hmul2_u(hsub2_u((t01 & 0x000F000Fu) | 0x64006400u, Zlo[b]), S2[2 * b]);
-                a[1] = hmul2_u(hsub2_u((t01 & 0x00F000F0u) | 0x54005400u, Zhi[b]), S2[2 * b + 1]);
-                a[2] = hmul2_u(hsub2_u((t89 & 0x000F000Fu) | 0x64006400u, Zlo[b]), S2[2 * b]);
-                a[3] = hmul2_u(hsub2_u((t89 & 0x00F000F0u) | 0x54005400u, Zhi[b]), S2[2 * b + 1]);
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) ptx::mma_16816(acc[b][mt], a, bf[mt][0], bf[mt][1]);
             }
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(empty + s));
 
         if (i == n_iters - 1 || kb == p.kiters - 1) {
-            // ---- segment end: fold k-groups 1..3 into k-group 0, in that order
-            if (kg > 0) {
-                float *dst = red + (kg - 1) * (MT * 16 * 128);
-#pragma unroll
-                for (int b = 0; b < 4; ++b)
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) dst[((b * MT + mt) * 4 + e) * 128 + ct] = acc[b][mt][e];
+            // ---- segment end: fold the k-groups into group 0, in the fixed
+            //      order (g0 + g2) + (g1 + g3) for four groups
+            if (KG == 4) {
+                if (kg >= 2) fold_store<MT>(red + (kg - 2) * kFoldFloats, acc, ct);
+                ptx::named_barrier(1, kConsumerThreads);
+                if (kg < 2) fold_add<MT>(red + kg * kFoldFloats, acc, ct);
+                ptx::named_barrier(1, kConsumerThreads);
             }
+            if (kg == 1) fold_store<MT>(red, acc, ct);
             ptx::named_barrier(1, kConsumerThreads);
-            if (kg == 0) {
-#pragma unroll 1
-                for (int src = 0; src < kKGroups - 1; ++src) {
-                    const float *from = red + src * (MT * 16 * 128);
-#pragma unroll
-                    for (int b = 0; b < 4; ++b)
-#pragma unroll
-                        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) acc[b][mt][e] += from[((b * MT + mt) * 4 + e) * 128 + ct];
-                }
-            }
+            if (kg == 0) fold_add<MT>(red, acc, ct);
             ptx::named_barrier(1, kConsumerThreads);
 
             // `whole` is uniform across the CTA; barrier participation never
@@ -332,12 +390,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 if (whole && live) {
                     float bv[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) bv[j] = 0.f;
+                    for (int jj = 0; jj < 8; ++jj) bv[jj] = 0.f;
                     if (p.bias && col0 < p.N) {
                         const uint4 braw = *reinterpret_cast<const uint4 *>(p.bias + col0);
                         const __half *bh = reinterpret_cast<const __half *>(&braw);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) bv[j] = __half2float(bh[j]);
+                        for (int jj = 0; jj < 8; ++jj) bv[jj] = __half2float(bh[jj]);
                     }
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt)
@@ -374,12 +432,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                     __threadfence();
                 }
                 if (!whole) {
-                    ptx::named_barrier(2, kConsumerThreads / kKGroups);
+                    ptx::named_barrier(2, kConsumerThreads / KG);
                     if (ct == 0 && !*abort_flag) atomicAdd(p.arrive + tile, 1u);
                 }
             }
             if (!whole) duty_tiles[duty_tiles[0] < 0 ? 0 : 1] = tile;
         }
+        if (++kb == p.kiters) { kb = 0; ++tile; }
     }
 
     // ---- reduction duties: every split tile this CTA helped with
@@ -425,25 +484,25 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 const int64_t inner = (int64_t)m * kTileCols + w * 8;
                 float s8[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) s8[j] = 0.f;
+                for (int jj = 0; jj < 8; ++jj) s8[jj] = 0.f;
                 // contributors in ascending order; loads issued 4 at a time
                 for (int cc = cf; cc <= cl; cc += 4) {
                     float4 lo[4], hi[4];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if (cc + j <= cl) {
-                            const int slot = 2 * (cc + j) + ((cc + j) == cf ? which_cf : 0);
+                    for (int jj = 0; jj < 4; ++jj) {
+                        if (cc + jj <= cl) {
+                            const int slot = 2 * (cc + jj) + ((cc + jj) == cf ? which_cf : 0);
                             const float4 *src = reinterpret_cast<const float4 *>(
                                 p.partials + (int64_t)slot * kPartialFloats + inner);
-                            lo[j] = __ldcg(src);
-                            hi[j] = __ldcg(src + 1);
+                            lo[jj] = __ldcg(src);
+                            hi[jj] = __ldcg(src + 1);
                         }
                     }
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if (cc + j <= cl) {
-                            s8[0] += lo[j].x; s8[1] += lo[j].y; s8[2] += lo[j].z; s8[3] += lo[j].w;
-                            s8[4] += hi[j].x; s8[5] += hi[j].y; s8[6] += hi[j].z; s8[7] += hi[j].w;
+                    for (int jj = 0; jj < 4; ++jj) {
+                        if (cc + jj <= cl) {
+                            s8[0] += lo[jj].x; s8[1] += lo[jj].y; s8[2] += lo[jj].z; s8[3] += lo[jj].w;
+                            s8[4] += hi[jj].x; s8[5] += hi[jj].y; s8[6] += hi[jj].z; s8[7] += hi[jj].w;
                         }
                     }
                 }
@@ -452,10 +511,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                     const uint4 braw = *reinterpret_cast<const uint4 *>(p.bias + col0);
                     const __half *bh = reinterpret_cast<const __half *>(&braw);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) out[j] = __float2half_rn(s8[j] + __half2float(bh[j]));
+                    for (int jj = 0; jj < 8; ++jj) out[jj] = __float2half_rn(s8[jj] + __half2float(bh[jj]));
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) out[j] = __float2half_rn(s8[j]);
+                    for (int jj = 0; jj < 8; ++jj) out[jj] = __float2half_rn(s8[jj]);
                 }
                 *reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.N + col0) = *reinterpret_cast<const uint4 *>(out);
             }
@@ -490,27 +549,54 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
-bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
-                 uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
-                 CUtensorMapSwizzle swizzle)
+// rank-2 or rank-3 tiled map; dims/box innermost first, strides in bytes for
+// dims 1.. (rank - 1 entries)
+bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, int rank,
+              const uint64_t *dims, const uint64_t *strides, const uint32_t *box,
+              CUtensorMapSwizzle swizzle)
 {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {box_inner, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+    cuuint64_t d[3], st[2];
+    cuuint32_t b[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+    }
+    for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
+    return enc(m, dt, (cuuint32_t)rank, const_cast<void *>(base), d, st, b, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Largest number of groups one 64-row stage can touch.
+// Largest number of groups one stage can touch.
 int group_rows_per_stage(int64_t g)
 {
     if (kStageRows % g == 0) return (int)(kStageRows / g);
     if (g % kStageRows == 0) return 1;
     return (int)((kStageRows - 1) / g + 2);
+}
+
+// The four tensor maps of a launch and the bytes one stage delivers.
+bool build_maps(const Problem &pr, int mpad, CUtensorMap *tw, CUtensorMap *tx, CUtensorMap *ts,
+                CUtensorMap *tz, uint32_t *stage_tx)
+{
+    const uint64_t K = (uint64_t)pr.K, N = (uint64_t)pr.N, M = (uint64_t)pr.M, G = (uint64_t)pr.G;
+    const int R = group_rows_per_stage(pr.g);
+    const uint64_t wd[2] = {N / 8, K}, ws[1] = {N / 2};
+    const uint32_t wb[2] = {kTileWords, kStageRows};
+    // x viewed as [M][K / 64][64]: one box covers a stage's 256 k for every token
+    const uint64_t xd[3] = {64, K / 64, M}, xs[2] = {128, K * 2};
+    const uint32_t xb[3] = {64, kKBlocks, (uint32_t)mpad};
+    const uint64_t sd[2] = {N, G}, ss[1] = {N * 2};
+    const uint32_t sb[2] = {kTileCols, (uint32_t)R};
+    const uint64_t zd[2] = {N / 8, G}, zs[1] = {N / 2};
+    const uint32_t zb[2] = {kTileWords, (uint32_t)R};
+    *stage_tx = (uint32_t)(kWBytes + mpad * kStageRows * 2 + R * (kTileCols * 2) + R * (kTileWords * 4));
+    return make_map(tw, CU_TENSOR_MAP_DATA_TYPE_INT32, pr.qweight, 2, wd, ws, wb, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.x, 3, xd, xs, xb, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.scales, 2, sd, ss, sb, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           make_map(tz, CU_TENSOR_MAP_DATA_TYPE_INT32, pr.qzeros, 2, zd, zs, zb, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // Per (device, kernel variant): dynamic shared memory opted in once, and the
@@ -521,7 +607,7 @@ struct LaunchInfo {
     cudaError_t err = cudaSuccess;
 };
 
-template <int MT>
+template <int MT, int KG, bool WG>
 LaunchInfo launch_info()
 {
     static std::mutex mu;
@@ -533,60 +619,46 @@ LaunchInfo launch_info()
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(dev);
     if (it != cache.end()) return it->second;
-    auto kern = decode_kernel<MT>;
+    auto kern = decode_kernel<MT, KG, WG>;
     li.err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (li.err == cudaSuccess)
         li.err = cudaDeviceGetAttribute(&li.sms, cudaDevAttrMultiProcessorCount, dev);
     if (li.err == cudaSuccess)
-        li.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&li.occ, kern, kThreads, kSmemBytes);
+        li.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&li.occ, kern, Layout<KG>::kThreads, kSmemBytes);
     if (li.err == cudaSuccess && li.occ < 1) li.err = cudaErrorLaunchOutOfResources;
     if (li.err == cudaSuccess) cache[dev] = li;
     return li;
 }
 
-template <int MT>
-cudaError_t launch_decode_t(const Problem &pr, cudaStream_t stream)
+// Fills everything but the scratch pointers; the grid size goes to p->ctas.
+template <int MT, int KG, bool WG>
+cudaError_t prepare(const Problem &pr, int max_ctas, CUtensorMap *maps, DecodeParams *p)
 {
-    const LaunchInfo li = launch_info<MT>();
+    const LaunchInfo li = launch_info<MT, KG, WG>();
     if (li.err != cudaSuccess) return li.err;
-
-    const int M = (int)pr.M, K = (int)pr.K, N = (int)pr.N, g = (int)pr.g;
-    const int tiles = (N + kTileCols - 1) / kTileCols;
-    const int kiters = (K + kStageRows - 1) / kStageRows;
+    const int tiles = (int)((pr.N + kTileCols - 1) / kTileCols);
+    const int kiters = (int)((pr.K + kStageRows - 1) / kStageRows);
     const int64_t total = (int64_t)tiles * kiters;
-    const int ctas = (int)std::min<int64_t>(total, (int64_t)li.occ * li.sms);
-    const int R = group_rows_per_stage(g);
-    const int mpad = 8 * MT;
+    const int ctas = (int)std::min<int64_t>(std::min<int64_t>(total, (int64_t)li.occ * li.sms), max_ctas);
+    uint32_t stage_tx = 0;
+    if (!build_maps(pr, 8 * MT, &maps[0], &maps[1], &maps[2], &maps[3], &stage_tx))
+        return cudaErrorInvalidValue;
+    *p = DecodeParams{};
+    p->bias = static_cast<const __half *>(pr.bias);
+    p->y = static_cast<__half *>(pr.y);
+    p->status = device_status_word();
+    p->M = (int)pr.M; p->K = (int)pr.K; p->N = (int)pr.N; p->g = (int)pr.g;
+    p->tiles = tiles; p->kiters = kiters; p->total = (int)total; p->ctas = ctas;
+    p->stage_tx = stage_tx;
+    return cudaSuccess;
+}
 
-    Scratch sc{};
-    if (!get_scratch(stream, (size_t)2 * ctas * kPartialFloats, (size_t)2 * tiles, &sc))
-        return cudaErrorMemoryAllocation;
-
-    CUtensorMap tw, tx, ts, tz;
-    bool ok = make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_INT32, pr.qweight, N / 8, K, (uint64_t)N / 2,
-                          kTileWords, kStageRows, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.x, K, M, (uint64_t)K * 2,
-                          kStageRows, mpad, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.scales, N, pr.G, (uint64_t)N * 2,
-                          kTileCols, R, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_INT32, pr.qzeros, N / 8, pr.G, (uint64_t)N / 2,
-                          kTileWords, R, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (!ok) return cudaErrorInvalidValue;
-
-    DecodeParams p{};
-    p.bias = static_cast<const __half *>(pr.bias);
-    p.y = static_cast<__half *>(pr.y);
-    p.partials = sc.partials;
-    p.arrive = sc.counters;
-    p.depart = sc.counters + tiles;
-    p.status = device_status_word();
-    p.M = M; p.K = K; p.N = N; p.g = g;
-    p.tiles = tiles; p.kiters = kiters; p.total = (int)total; p.ctas = ctas;
-    p.stage_tx = (uint32_t)(kWBytes + mpad * 128 + R * (kTileCols * 2) + R * (kTileWords * 4));
-
+template <int MT, int KG, bool WG>
+cudaError_t launch_kernel(const CUtensorMap *maps, const DecodeParams &p, cudaStream_t stream)
+{
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)ctas);
-    cfg.blockDim = dim3(kThreads);
+    cfg.gridDim = dim3((unsigned)p.ctas);
+    cfg.blockDim = dim3(Layout<KG>::kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -594,24 +666,55 @@ cudaError_t launch_decode_t(const Problem &pr, cudaStream_t stream)
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<MT>, tw, tx, ts, tz, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<MT, KG, WG>, maps[0], maps[1], maps[2], maps[3], p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+template <int MT, int KG, bool WG>
+cudaError_t launch_decode_t(const Problem &pr, cudaStream_t stream)
+{
+    CUtensorMap maps[4];
+    DecodeParams p;
+    cudaError_t e = prepare<MT, KG, WG>(pr, 1 << 30, maps, &p);
+    if (e != cudaSuccess) return e;
+    Scratch sc{};
+    if (!get_scratch(stream, (size_t)2 * p.ctas * kPartialFloats, (size_t)2 * p.tiles, &sc))
+        return cudaErrorMemoryAllocation;
+    p.partials = sc.partials;
+    p.arrive = sc.counters;
+    p.depart = sc.counters + p.tiles;
+    return launch_kernel<MT, KG, WG>(maps, p, stream);
+}
+
+// Consumer k-groups. Two (8 consumer warps + the producer, up to 168
+// registers a thread) ran a little faster than four (16 + 1 warps, held to
+// 96 registers, which spilled at two token tiles) for every decode shape.
+template <int MT> struct KGroupsFor { static constexpr int value = 2; };
+
+// whole: g divides the rows each warp takes per stage into one group
+template <int MT>
+cudaError_t dispatch_decode(const Problem &p, cudaStream_t stream)
+{
+    constexpr int KG = KGroupsFor<MT>::value;
+    const bool whole = p.g % Layout<KG>::kRowsPerWarp == 0;
+    return whole ? launch_decode_t<MT, KG, true>(p, stream) : launch_decode_t<MT, KG, false>(p, stream);
 }
 
 } // namespace
 
 bool decode_supported(int64_t M, int64_t K, int64_t N, int64_t g)
 {
-    return M >= 1 && M <= kMaxTokens && K % 16 == 0 && N % 32 == 0 && g % 16 == 0 &&
-           K <= (int64_t(1) << 30) && N <= (int64_t(1) << 30) &&
+    return M >= 1 && M <= kMaxTokens && K % 64 == 0 && N % 32 == 0 && g % 16 == 0 &&
+           group_rows_per_stage(g) <= kMaxGroupRows && K <= (int64_t(1) << 30) &&
+           N <= (int64_t(1) << 30) &&
            ((K + kStageRows - 1) / kStageRows) * ((N + kTileCols - 1) / kTileCols) < (int64_t(1) << 31);
 }
 
 cudaError_t launch_decode(const Problem &p, cudaStream_t stream)
 {
     if (!decode_supported(p.M, p.K, p.N, p.g)) return cudaErrorInvalidValue;
-    return p.M <= 8 ? launch_decode_t<1>(p, stream) : launch_decode_t<2>(p, stream);
+    return p.M <= 8 ? dispatch_decode<1>(p, stream) : dispatch_decode<2>(p, stream);
 }
 
 } // namespace awq
@@ -661,61 +764,30 @@ cudaError_t noalloc_scratch_address(uint32_t **out)
     return cudaSuccess;
 }
 
-template <int MT>
+template <int MT, int KG, bool WG>
 cudaError_t launch_decode_noalloc_t(const Problem &pr, cudaStream_t stream, uint32_t *scratch)
 {
-    const LaunchInfo li = launch_info<MT>();
-    if (li.err != cudaSuccess) return li.err;
-
-    const int M = (int)pr.M, K = (int)pr.K, N = (int)pr.N, g = (int)pr.g;
-    const int tiles = (N + kTileCols - 1) / kTileCols;
-    const int kiters = (K + kStageRows - 1) / kStageRows;
-    const int64_t total = (int64_t)tiles * kiters;
-    const int ctas = (int)std::min<int64_t>(std::min<int64_t>(total, (int64_t)li.occ * li.sms),
-                                            kNoAllocMaxCtas);
-    const int R = group_rows_per_stage(g);
-    const int mpad = 8 * MT;
-
-    CUtensorMap tw, tx, ts, tz;
-    bool ok = make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_INT32, pr.qweight, N / 8, K, (uint64_t)N / 2,
-                          kTileWords, kStageRows, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.x, K, M, (uint64_t)K * 2,
-                          kStageRows, mpad, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.scales, N, pr.G, (uint64_t)N * 2,
-                          kTileCols, R, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_INT32, pr.qzeros, N / 8, pr.G, (uint64_t)N / 2,
-                          kTileWords, R, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (!ok) return cudaErrorInvalidValue;
-
-    DecodeParams p{};
-    p.bias = static_cast<const __half *>(pr.bias);
-    p.y = static_cast<__half *>(pr.y);
+    CUtensorMap maps[4];
+    DecodeParams p;
+    cudaError_t e = prepare<MT, KG, WG>(pr, kNoAllocMaxCtas, maps, &p);
+    if (e != cudaSuccess) return e;
     p.partials = reinterpret_cast<float *>(scratch);
     p.arrive = scratch + kNoAllocPartialWords;
-    p.depart = p.arrive + tiles;
-    p.status = device_status_word();
-    p.M = M; p.K = K; p.N = N; p.g = g;
-    p.tiles = tiles; p.kiters = kiters; p.total = (int)total; p.ctas = ctas;
-    p.stage_tx = (uint32_t)(kWBytes + mpad * 128 + R * (kTileCols * 2) + R * (kTileWords * 4));
-
+    p.depart = p.arrive + p.tiles;
     // the array keeps whatever the previous call left: the counters must
     // start at zero (the partial slots are always written before being read)
-    cudaError_t e = cudaMemsetAsync(p.arrive, 0, sizeof(uint32_t) * 2 * (size_t)tiles, stream);
+    e = cudaMemsetAsync(p.arrive, 0, sizeof(uint32_t) * 2 * (size_t)p.tiles, stream);
     if (e != cudaSuccess) return e;
+    return launch_kernel<MT, KG, WG>(maps, p, stream);
+}
 
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)ctas);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, decode_kernel<MT>, tw, tx, ts, tz, p);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+template <int MT>
+cudaError_t dispatch_noalloc(const Problem &p, cudaStream_t stream, uint32_t *scratch)
+{
+    constexpr int KG = KGroupsFor<MT>::value;
+    const bool whole = p.g % Layout<KG>::kRowsPerWarp == 0;
+    return whole ? launch_decode_noalloc_t<MT, KG, true>(p, stream, scratch)
+                 : launch_decode_noalloc_t<MT, KG, false>(p, stream, scratch);
 }
 
 bool aligned16_ptr(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -743,7 +815,7 @@ extern "C" awq_status_t awq_linear_forward_decode_noalloc(
     if (awq::noalloc_scratch_address(&scratch) != cudaSuccess) return AWQ_ERR_CUDA;
     awq::Problem p{x, qweight, qzeros, scales, bias, y, M, K, N, g, K / g};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = (M <= 8) ? awq::launch_decode_noalloc_t<1>(p, s, scratch)
-                                   : awq::launch_decode_noalloc_t<2>(p, s, scratch);
+    const cudaError_t e = (M <= 8) ? awq::dispatch_noalloc<1>(p, s, scratch)
+                                   : awq::dispatch_noalloc<2>(p, s, scratch);
     return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
 }

@@ -84,14 +84,19 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Tests the phase; if it has not completed, the thread is suspended until it
+// does or until about `hint_ns` nanoseconds pass, so a waiting thread does
+// not spin and take issue slots from the warps doing the work.
+constexpr uint32_t kSuspendHintNs = 1000000u;   // 1 ms
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
@@ -109,15 +114,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int *abort, unsigned int *status) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    for (uint32_t n = 1;; ++n) {
+    while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 255u) == 0) {
-            if (abort && *abort) return false;
-            if (clock64() - t0 > kWaitLimitCycles) {
-                if (abort) *abort = 1;
-                if (status) atomicOr(status, 1u);
-                return false;
-            }
+        if (abort && *abort) return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            if (abort) *abort = 1;
+            if (status) atomicOr(status, 1u);
+            return false;
         }
     }
 }
@@ -134,6 +137,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+// 3-D tiled TMA load global -> shared; coordinates innermost first.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint32_t bar,
+                                            int32_t c0, int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
 

@@ -117,8 +117,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                const PrefillParams p)
 {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // round up to 1024 bytes by offsetting the shared array itself, so that
+    // the compiler still knows every derived pointer is a shared address
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kBarOff);
     uint64_t *dqd = full + kStages;        // dequantised B ready
     uint64_t *empty = dqd + kStages;       // MMAs of the stage done
