@@ -28,12 +28,18 @@
 //    into the fraction of 1024.0 or 64.0, an exact half2 subtract removes the
 //    zero point and one half2 multiply (round to nearest) applies the scale --
 //    exactly fp16_rn((q - z) s).
-//  * Reduction: a tile split between CTAs is summed by its contributors
-//    together at the end of the kernel: each writes its fp32 partial to
-//    scratch and counts itself in; after its own stream is done it waits
-//    (bounded) for the count and then reduces a slice of the tile, in the
-//    fixed contributor order, adding the bias and rounding once. The grid is
-//    launched cooperatively so that every CTA is resident.
+//  * Reduction: a tile split between CTAs is finished by the CTA that holds
+//    its last k-stages, which is the highest-numbered contributor (its range
+//    starts inside the tile). Every contributor writes its fp32 partial to
+//    scratch; the others count themselves in, and after its own stream the
+//    finisher waits (bounded) for them -- only ever for lower-numbered CTAs,
+//    which were dispatched before it, so no co-residency is needed -- pulls
+//    all partials into its idle stage ring with bulk copies, sums them in
+//    contributor order, adds the bias and rounds once.
+//  * Launch: programmatic dependent launch. The kernel lets the next one be
+//    scheduled at once and loads its first stages' weights before waiting
+//    for the previous kernel; activations, bias, output and scratch are
+//    touched only after that wait.
 //
 // Requirements (else another path serves): 1 <= M <= 16, K % 64 == 0,
 // N % 32 == 0 (TMA row pitch), g % 16 == 0 with at most 8 groups per 256-row
@@ -97,7 +103,6 @@ struct DecodeParams {
     __half *y;
     float *partials;        // [2 * ctas][16][256]
     unsigned int *arrive;   // [tiles]
-    unsigned int *depart;   // [tiles]
     unsigned int *status;
     int M, K, N, g;
     int tiles, kiters, total, ctas;
@@ -154,7 +159,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     float *red = reinterpret_cast<float *>(smem + kRedOff);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kBarOff);
     uint64_t *empty = full + kStages;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStages);
+    uint64_t *gather = empty + kStages;   // partials of a split tile, see the end
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gather + 1);
     volatile int *duty_ok = abort_flag + 1;
     volatile uint32_t *consts = reinterpret_cast<volatile uint32_t *>(abort_flag + 2);
 
@@ -169,12 +175,21 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     const int begin = range_begin(c, p.total, p.ctas);
     const int end = range_begin(c + 1, p.total, p.ctas);
     const int n_iters = end - begin;
+    const int first_tile = begin / p.kiters;
+    // This CTA finishes the tile its range starts in when the range starts
+    // inside that tile and reaches the tile's last k-stage: the other
+    // contributors are then lower-numbered CTAs, which started before it.
+    const bool reducer = n_iters > 0 && begin % p.kiters != 0 && end >= (first_tile + 1) * p.kiters;
+
+    // the next kernel on the stream may be scheduled as SMs free up
+    ptx::launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(ptx::smem_addr(full + s), 1);
             ptx::mbar_init(ptx::smem_addr(empty + s), kConsumerWarps);
         }
+        ptx::mbar_init(ptx::smem_addr(gather), 1);
         *abort_flag = 0;
         *duty_ok = 0;
         consts[0] = 0x64006400u;   // 1024.0 in both halves
@@ -190,10 +205,31 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             ptx::prefetch_tmap(&tm_x);
             ptx::prefetch_tmap(&tm_s);
             ptx::prefetch_tmap(&tm_z);
-            int issued = 0;
-            int tile = begin / p.kiters;
+            int tile = first_tile;
             int kb = begin - tile * p.kiters;
-            for (int i = 0; i < n_iters; ++i) {
+            // The weights, scales and zero points of the first stages do not
+            // depend on the kernel before this one: load them while it
+            // finishes, and the activations once it has.
+            const int pre = n_iters < kStages ? n_iters : kStages;
+            for (int i = 0; i < pre; ++i) {
+                const uint32_t fb = ptx::smem_addr(full + i);
+                const uint32_t st = ptx::smem_addr(smem + i * kStageBytes);
+                const int k0 = kb * kStageRows;
+                const int grp0 = k0 / p.g;
+                ptx::mbar_arrive_expect_tx(fb, p.stage_tx);
+                ptx::tma_load_2d(st, &tm_w, fb, tile * kTileWords, k0);
+                ptx::tma_load_2d(st + kSOff, &tm_s, fb, tile * kTileCols, grp0);
+                ptx::tma_load_2d(st + kZOff, &tm_z, fb, tile * kTileWords, grp0);
+                if (++kb == p.kiters) { kb = 0; ++tile; }
+            }
+            ptx::wait_prerequisites();
+            for (int i = 0, kx = begin % p.kiters; i < pre; ++i) {
+                ptx::tma_load_3d(ptx::smem_addr(smem + i * kStageBytes + kXOff), &tm_x,
+                                 ptx::smem_addr(full + i), 0, kx * (kStageRows / 64), 0);
+                if (++kx == p.kiters) kx = 0;
+            }
+            int issued = pre;
+            for (int i = pre; i < n_iters; ++i) {
                 const int s = i % kStages;
                 const uint32_t parity = ((i / kStages) & 1) ^ 1;
                 if (!ptx::mbar_wait_bounded(ptx::smem_addr(empty + s), parity, abort_flag, p.status))
@@ -221,6 +257,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     }
 
     // ------------------------------------------------------------------ consumers
+    // everything below reads or writes global memory the kernel before this
+    // one may still use (activations come through the producer, which waited)
+    ptx::wait_prerequisites();
     const int kg = warp / kColWarps;   // rows kRowsPerWarp * kg .. of every stage
     const int cw = warp % kColWarps;   // which 64-column quarter of the tile
     const int gq = lane >> 2;          // MMA groupID: output column pair / token
@@ -266,8 +305,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     // and of this warp's first row (wg_)
     int st_grp = 0, st_rem = 0, wg_grp = 0, wg_rem = 0;
     int seg_kb0 = 0;
-    int duty_tiles[2] = {-1, -1};
-    const int first_tile = begin / p.kiters;
     int tile = first_tile;
     int kb = begin - tile * p.kiters;
 
@@ -433,101 +470,110 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 }
                 if (!whole) {
                     ptx::named_barrier(2, kConsumerThreads / KG);
-                    if (ct == 0 && !*abort_flag) atomicAdd(p.arrive + tile, 1u);
+                    // count in with the tile's finisher (not needed for its own tile)
+                    if (ct == 0 && !*abort_flag && !(reducer && tile == first_tile))
+                        atomicAdd(p.arrive + tile, 1u);
                 }
             }
-            if (!whole) duty_tiles[duty_tiles[0] < 0 ? 0 : 1] = tile;
         }
         if (++kb == p.kiters) { kb = 0; ++tile; }
     }
 
-    // ---- reduction duties: every split tile this CTA helped with
+    // ---- finishing the split tile this range starts in: wait for the other
+    //      contributors (lower-numbered CTAs) to count in, bring every
+    //      partial, its own included, into the now idle stage ring with bulk
+    //      copies, and sum them in contributor order, so the result does not
+    //      depend on timing; then add the bias and round once.
+    if (!reducer) return;
     const int ctid = threadIdx.x;   // 0 .. kConsumerThreads-1
-#pragma unroll 1
-    for (int d = 0; d < 2; ++d) {
-        const int t = duty_tiles[d];
-        if (t < 0) break;
-        const int cf = cta_of(t * p.kiters, p.total, p.ctas);
-        const int cl = cta_of((t + 1) * p.kiters - 1, p.total, p.ctas);
-        const int n = cl - cf + 1;
-        // every contributor after the first starts inside tile t, so its
-        // partial of t is in its first slot; the first one may have started
-        // in an earlier tile
-        const int which_cf = (range_begin(cf, p.total, p.ctas) / p.kiters == t) ? 0 : 1;
+    const int t = first_tile;
+    const int cf = cta_of(t * p.kiters, p.total, p.ctas);
+    const int n = c - cf + 1;
+    if (ctid == 0) {
+        bool ok = !*abort_flag;
+        const long long t0 = clock64();
+        while (ok && ptx::ld_acquire_gpu(p.arrive + t) < (unsigned)(n - 1)) {
+            if (*abort_flag || clock64() - t0 > ptx::kWaitLimitCycles) {
+                ok = false;
+                *abort_flag = 1;
+                atomicOr(p.status, kStatusTimeout);
+            } else {
+                __nanosleep(32);
+            }
+        }
+        *duty_ok = ok ? 1 : 0;
+    }
+    ptx::named_barrier(1, kConsumerThreads);
+    if (!*duty_ok) return;
+    constexpr int kUnits = (kMaxTokens * kTileWords + kConsumerThreads - 1) / kConsumerThreads;
+    const uint32_t slot_bytes = (uint32_t)p.M * kTileCols * 4;
+    const int per_round = (int)((uint32_t)(kStages * kStageBytes) / slot_bytes);
+    const int units = p.M * kTileWords;   // (token, packed word) pairs of the tile
+    float sum[kUnits][8];
+#pragma unroll
+    for (int q = 0; q < kUnits; ++q)
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) sum[q][jj] = 0.f;
+    bool ok = true;
+    for (int r0 = 0, round = 0; r0 < n; r0 += per_round, ++round) {
+        const int cnt = std::min(per_round, n - r0);
+        if (round > 0) ptx::named_barrier(1, kConsumerThreads);   // last round's reads are done
         if (ctid == 0) {
-            bool ok = !*abort_flag;
-            if (ok) {
-                const long long t0 = clock64();
-                while (ptx::ld_acquire_gpu(p.arrive + t) < (unsigned)n) {
-                    if (*abort_flag || clock64() - t0 > ptx::kWaitLimitCycles) {
-                        ok = false;
-                        *abort_flag = 1;
-                        atomicOr(p.status, kStatusTimeout);
-                        break;
-                    }
-                    __nanosleep(32);
-                }
-            }
-            *duty_ok = ok ? 1 : 0;
-        }
-        ptx::named_barrier(1, kConsumerThreads);
-        if (*duty_ok) {
-            const int units = p.M * kTileWords;          // (token, word) pairs of the tile
-            const int i = c - cf;
-            const int u0 = (int)((int64_t)i * units / n);
-            const int u1 = (int)((int64_t)(i + 1) * units / n);
-            for (int u = u0 + ctid; u < u1; u += kConsumerThreads) {
-                const int m = u / kTileWords;
-                const int w = u - m * kTileWords;
-                const int col0 = t * kTileCols + w * 8;
-                if (col0 >= p.N) continue;
-                const int64_t inner = (int64_t)m * kTileCols + w * 8;
-                float s8[8];
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) s8[jj] = 0.f;
-                // contributors in ascending order; loads issued 4 at a time
-                for (int cc = cf; cc <= cl; cc += 4) {
-                    float4 lo[4], hi[4];
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        if (cc + jj <= cl) {
-                            const int slot = 2 * (cc + jj) + ((cc + jj) == cf ? which_cf : 0);
-                            const float4 *src = reinterpret_cast<const float4 *>(
-                                p.partials + (int64_t)slot * kPartialFloats + inner);
-                            lo[jj] = __ldcg(src);
-                            hi[jj] = __ldcg(src + 1);
-                        }
-                    }
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        if (cc + jj <= cl) {
-                            s8[0] += lo[jj].x; s8[1] += lo[jj].y; s8[2] += lo[jj].z; s8[3] += lo[jj].w;
-                            s8[4] += hi[jj].x; s8[5] += hi[jj].y; s8[6] += hi[jj].z; s8[7] += hi[jj].w;
-                        }
-                    }
-                }
-                __align__(16) __half out[8];
-                if (p.bias) {
-                    const uint4 braw = *reinterpret_cast<const uint4 *>(p.bias + col0);
-                    const __half *bh = reinterpret_cast<const __half *>(&braw);
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) out[jj] = __float2half_rn(s8[jj] + __half2float(bh[jj]));
-                } else {
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) out[jj] = __float2half_rn(s8[jj]);
-                }
-                *reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.N + col0) = *reinterpret_cast<const uint4 *>(out);
+            // the partials were written through the generic proxy (and
+            // acquired above); the bulk copies read them through the async one
+            ptx::fence_proxy_async();
+            ptx::mbar_arrive_expect_tx(ptx::smem_addr(gather), (uint32_t)cnt * slot_bytes);
+            for (int q = 0; q < cnt; ++q) {
+                const int cc = cf + r0 + q;
+                const int which = (range_begin(cc, p.total, p.ctas) / p.kiters == t) ? 0 : 1;
+                ptx::bulk_load(ptx::smem_addr(smem + q * slot_bytes),
+                               p.partials + (int64_t)(2 * cc + which) * kPartialFloats, slot_bytes,
+                               ptx::smem_addr(gather));
             }
         }
-        ptx::named_barrier(1, kConsumerThreads);
-        if (ctid == 0 && *duty_ok) {
-            // last one out resets the tile's counters for the next call
-            if (atomicAdd(p.depart + t, 1u) == (unsigned)(n - 1)) {
-                atomicExch(p.arrive + t, 0u);
-                atomicExch(p.depart + t, 0u);
+        ok = ptx::mbar_wait_bounded(ptx::smem_addr(gather), (uint32_t)(round & 1), nullptr, p.status) && ok;
+        if (ok) {
+#pragma unroll
+            for (int q = 0; q < kUnits; ++q) {
+                const int u = ctid + q * kConsumerThreads;
+                if (u < units) {
+                    const int m = u / kTileWords;
+                    const int w = u - m * kTileWords;
+                    const float *src = reinterpret_cast<const float *>(smem) + m * kTileCols + w * 8;
+                    for (int cc = 0; cc < cnt; ++cc) {
+                        const float4 lo = *reinterpret_cast<const float4 *>(src + cc * (slot_bytes / 4));
+                        const float4 hi = *reinterpret_cast<const float4 *>(src + cc * (slot_bytes / 4) + 4);
+                        sum[q][0] += lo.x; sum[q][1] += lo.y; sum[q][2] += lo.z; sum[q][3] += lo.w;
+                        sum[q][4] += hi.x; sum[q][5] += hi.y; sum[q][6] += hi.z; sum[q][7] += hi.w;
+                    }
+                }
             }
         }
     }
+    if (ok && !*abort_flag) {
+#pragma unroll
+        for (int q = 0; q < kUnits; ++q) {
+            const int u = ctid + q * kConsumerThreads;
+            if (u >= units) continue;
+            const int m = u / kTileWords;
+            const int w = u - m * kTileWords;
+            const int col0 = t * kTileCols + w * 8;
+            if (col0 >= p.N) continue;
+            __align__(16) __half out[8];
+            if (p.bias) {
+                const uint4 braw = *reinterpret_cast<const uint4 *>(p.bias + col0);
+                const __half *bh = reinterpret_cast<const __half *>(&braw);
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) out[jj] = __float2half_rn(sum[q][jj] + __half2float(bh[jj]));
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) out[jj] = __float2half_rn(sum[q][jj]);
+            }
+            *reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.N + col0) = *reinterpret_cast<const uint4 *>(out);
+        }
+    }
+    // the counter is this CTA's alone now: reset it for the next call
+    if (ctid == 0) atomicExch(p.arrive + t, 0u);
 }
 
 // ---------------------------------------------------------------------------
@@ -661,9 +707,12 @@ cudaError_t launch_kernel(const CUtensorMap *maps, const DecodeParams &p, cudaSt
     cfg.blockDim = dim3(Layout<KG>::kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
+    // programmatic dependent launch: the kernel starts streaming weights while
+    // the previous kernel on the stream drains (it waits for it before
+    // touching activations, bias, output or scratch)
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<MT, KG, WG>, maps[0], maps[1], maps[2], maps[3], p);
@@ -679,11 +728,10 @@ cudaError_t launch_decode_t(const Problem &pr, cudaStream_t stream)
     cudaError_t e = prepare<MT, KG, WG>(pr, 1 << 30, maps, &p);
     if (e != cudaSuccess) return e;
     Scratch sc{};
-    if (!get_scratch(stream, (size_t)2 * p.ctas * kPartialFloats, (size_t)2 * p.tiles, &sc))
+    if (!get_scratch(stream, (size_t)2 * p.ctas * kPartialFloats, (size_t)p.tiles, &sc))
         return cudaErrorMemoryAllocation;
     p.partials = sc.partials;
     p.arrive = sc.counters;
-    p.depart = sc.counters + p.tiles;
     return launch_kernel<MT, KG, WG>(maps, p, stream);
 }
 
@@ -733,11 +781,11 @@ namespace {
 constexpr int kNoAllocMaxCtas = 160;    // grid cap: partial slots for 160 CTAs
 constexpr int kNoAllocMaxTiles = 8192;  // 256-column tiles: N up to 2,097,152
 constexpr size_t kNoAllocPartialWords = (size_t)2 * kNoAllocMaxCtas * kPartialFloats;
-constexpr size_t kNoAllocWords = kNoAllocPartialWords + (size_t)2 * kNoAllocMaxTiles;
+constexpr size_t kNoAllocWords = kNoAllocPartialWords + (size_t)kNoAllocMaxTiles;
 
-// fp32 partials (2 slots per CTA) followed by the arrival and departure
-// counters of every tile: 5,242,880 + 65,536 bytes on every GPU that loads
-// this library, for as long as the library stays loaded.
+// fp32 partials (2 slots per CTA) followed by the arrival counter of every
+// tile: 5,242,880 + 32,768 bytes on every GPU that loads this library, for as
+// long as the library stays loaded.
 static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocWords];
 
 // Device address of g_noalloc_scratch on the current device. Host code only
@@ -773,10 +821,9 @@ cudaError_t launch_decode_noalloc_t(const Problem &pr, cudaStream_t stream, uint
     if (e != cudaSuccess) return e;
     p.partials = reinterpret_cast<float *>(scratch);
     p.arrive = scratch + kNoAllocPartialWords;
-    p.depart = p.arrive + p.tiles;
     // the array keeps whatever the previous call left: the counters must
     // start at zero (the partial slots are always written before being read)
-    e = cudaMemsetAsync(p.arrive, 0, sizeof(uint32_t) * 2 * (size_t)p.tiles, stream);
+    e = cudaMemsetAsync(p.arrive, 0, sizeof(uint32_t) * (size_t)p.tiles, stream);
     if (e != cudaSuccess) return e;
     return launch_kernel<MT, KG, WG>(maps, p, stream);
 }

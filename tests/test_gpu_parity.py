@@ -244,3 +244,44 @@ def test_library_cross_check_cublas(gpu):
     y = (pg.x.float() @ W.float() + pg.bias.float()).half()
     from parity import oracle_reference
     assert_close(y.cpu().numpy(), oracle_reference(p), "cuBLAS on awq_dequant")
+
+
+# --------------------------------------------------------------------------
+# back-to-back calls on one stream: each layer's output is the next one's
+# input, and a later layer writes the buffer an earlier one read. The decode
+# kernel may start streaming weights before the previous kernel has finished
+# (programmatic dependent launch); it must still see that kernel's output and
+# must not overwrite what it reads. The chained result has to equal, bit for
+# bit, the same calls with a device synchronisation after each.
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M", [1, 16])
+@pytest.mark.parametrize("path", [Path.DECODE, Path.AUTO])
+def test_chained_layers_match_serialised(gpu, M, path):
+    K = N = 2048
+    layers = [make_problem(M, K, N, 128, bias=(i == 1), seed=40 + i).to(torch.device("cuda"))
+              for i in range(4)]
+    x0 = make_activations(M, K, seed=7).cuda()
+
+    def run(sync: bool) -> list:
+        a = x0.clone()
+        b = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+        bufs, outs = [a, b], []
+        for i, L in enumerate(layers):
+            src, dst = bufs[i % 2], bufs[(i + 1) % 2]
+            linear_forward(src, L.qweight, L.qzeros, L.scales, L.bias, L.group_size, path=path, out=dst)
+            if sync:
+                torch.cuda.synchronize()
+                outs.append(dst.clone())
+        torch.cuda.synchronize()
+        return outs if sync else [bufs[len(layers) % 2].clone()]
+
+    serial = run(sync=True)
+    chained = run(sync=False)
+    assert torch.equal(chained[0].view(torch.int16), serial[-1].view(torch.int16))
+    # the first layer of the serial run against the oracle
+    p0 = layers[0]
+    ref = oracle.forward(x0.cpu().numpy(), p0.qweight.cpu().numpy(), p0.qzeros.cpu().numpy(),
+                         p0.scales.cpu().numpy(), None, p0.group_size)
+    assert_close(serial[0].cpu().numpy(), ref, "chained layer 0")
+    assert awq_last_device_status(torch.cuda.current_stream().cuda_stream) == 0
