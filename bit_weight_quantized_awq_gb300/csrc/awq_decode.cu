@@ -276,19 +276,23 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     const uint32_t rA = (uint32_t)(2 * tq), rB = rA + 1;
     const uint32_t offA = (uint32_t)R0 * 128 + rA * 128 + ((wchunk ^ rA) << 4) + inw;
     const uint32_t offB = (uint32_t)R0 * 128 + rB * 128 + ((wchunk ^ rB) << 4) + inw;
-    // activation slice: [token m][64-row block][64 halves], 128-byte rows;
-    // chunk j of this warp is in block R0 / 64 + j / 4, 16-byte units
-    // 2 (j % 4) and 2 (j % 4) + 1. The 128-byte swizzle XORs bits 4..6 of the
-    // offset, which are zero in the row base, so the address of unit u is
-    // (row base | phase) ^ (u << 4).
+    // activation slice: [token m][64-row block][64 halves], 128-byte rows
+    // (r = m * 4 + block), 16-byte unit u of row r stored at unit u ^ (r % 8).
+    // Chunk j of this warp is block R0 / 64 + j / 4, units 2 (j % 4) and
+    // 2 (j % 4) + 1 -- the k 0..7 and 8..15 halves of its B operand. One
+    // ldmatrix.x4 fetches the B operands of a chunk pair for eight tokens:
+    // lane L addresses token L % 8, unit 4 * pair + L / 8 of the block.
     constexpr int kBlocksPerWarp = (kChunksPerWarp + 3) / 4;
-    uint32_t xrow[MT][kBlocksPerWarp];
+    static_assert(kChunksPerWarp % 2 == 0, "chunks are fetched in pairs");
+    uint32_t xoff[MT][kBlocksPerWarp][2];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int jb = 0; jb < kBlocksPerWarp; ++jb) {
-            const uint32_t r = (uint32_t)((8 * mt + gq) * kKBlocks + R0 / 64 + jb);
-            xrow[mt][jb] = (kXOff + r * 128 + 4 * tq) | ((r & 7) << 4);
+            const uint32_t r = (uint32_t)((8 * mt + (lane & 7)) * kKBlocks + R0 / 64 + jb);
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr)
+                xoff[mt][jb][pr] = kXOff + r * 128 + (((uint32_t)(4 * pr + (lane >> 3)) ^ (r & 7)) << 4);
         }
     const uint32_t soff = kSOff + (uint32_t)word * 16;
     const uint32_t zoff = kZOff + (uint32_t)word * 4;
@@ -363,6 +367,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 }
             }
             int grp = wg_grp, rem = wg_rem;
+            const uint32_t sbase = ptx::smem_addr(stp);
+            uint32_t xq[MT][4];   // B operands of the current chunk pair
 #pragma unroll
             for (int j = 0; j < kChunksPerWarp; ++j) {
                 if (!kWholeGroups) {
@@ -380,11 +386,16 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 const uint32_t v1 = *reinterpret_cast<const uint32_t *>(wp + offB);
                 const uint32_t v8 = *reinterpret_cast<const uint32_t *>(wp + offA + 1024);
                 const uint32_t v9 = *reinterpret_cast<const uint32_t *>(wp + offB + 1024);
+                if ((j & 1) == 0) {
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt)
+                        ptx::ldmatrix_x4(sbase + xoff[mt][j / 4][(j % 4) / 2], xq[mt]);
+                }
                 uint32_t bf[MT][2];
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
-                    bf[mt][0] = *reinterpret_cast<const uint32_t *>(stp + (xrow[mt][j / 4] ^ (uint32_t)((2 * (j % 4)) << 4)));
-                    bf[mt][1] = *reinterpret_cast<const uint32_t *>(stp + (xrow[mt][j / 4] ^ (uint32_t)((2 * (j % 4) + 1) << 4)));
+                    bf[mt][0] = xq[mt][2 * (j & 1)];
+                    bf[mt][1] = xq[mt][2 * (j & 1) + 1];
                 }
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {

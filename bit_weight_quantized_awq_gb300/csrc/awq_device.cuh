@@ -153,11 +153,19 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
 // D(16x8, f32) += A(16x16, f16, row) * B(16x8, f16, col)
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                           uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four 8x8 b16 matrices from shared memory in the mma operand layout: lanes
+// 8i..8i+7 give the row addresses (16 bytes each) of matrix i; lane
+// (4 g + t) receives elements 2t, 2t+1 of row g of every matrix.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&d)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]) : "r"(addr) : "memory");
 }
 
 // Untiled bulk copy global -> shared (both 16-byte aligned, bytes % 16 == 0),
