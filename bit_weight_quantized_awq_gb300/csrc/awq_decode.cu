@@ -33,9 +33,8 @@
 //    starts inside the tile). Every contributor writes its fp32 partial to
 //    scratch; the others count themselves in, and after its own stream the
 //    finisher waits (bounded) for them -- only ever for lower-numbered CTAs,
-//    which were dispatched before it, so no co-residency is needed -- pulls
-//    all partials into its idle stage ring with bulk copies, sums them in
-//    contributor order, adds the bias and rounds once.
+//    which were dispatched before it, so no co-residency is needed -- sums
+//    all partials in contributor order, adds the bias and rounds once.
 //  * Launch: programmatic dependent launch. The kernel lets the next one be
 //    scheduled at once and loads its first stages' weights before waiting
 //    for the previous kernel; activations, bias, output and scratch are
@@ -159,8 +158,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     float *red = reinterpret_cast<float *>(smem + kRedOff);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kBarOff);
     uint64_t *empty = full + kStages;
-    uint64_t *gather = empty + kStages;   // partials of a split tile, see the end
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(gather + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStages);
     volatile int *duty_ok = abort_flag + 1;
     volatile uint32_t *consts = reinterpret_cast<volatile uint32_t *>(abort_flag + 2);
 
@@ -189,7 +187,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             ptx::mbar_init(ptx::smem_addr(full + s), 1);
             ptx::mbar_init(ptx::smem_addr(empty + s), kConsumerWarps);
         }
-        ptx::mbar_init(ptx::smem_addr(gather), 1);
         *abort_flag = 0;
         *duty_ok = 0;
         consts[0] = 0x64006400u;   // 1024.0 in both halves
@@ -491,10 +488,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     }
 
     // ---- finishing the split tile this range starts in: wait for the other
-    //      contributors (lower-numbered CTAs) to count in, bring every
-    //      partial, its own included, into the now idle stage ring with bulk
-    //      copies, and sum them in contributor order, so the result does not
-    //      depend on timing; then add the bias and round once.
+    //      contributors (lower-numbered CTAs) to count in, then sum every
+    //      partial, its own included, in contributor order, so the result
+    //      does not depend on timing; add the bias and round once.
     if (!reducer) return;
     const int ctid = threadIdx.x;   // 0 .. kConsumerThreads-1
     const int t = first_tile;
@@ -516,72 +512,63 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     }
     ptx::named_barrier(1, kConsumerThreads);
     if (!*duty_ok) return;
-    constexpr int kUnits = (kMaxTokens * kTileWords + kConsumerThreads - 1) / kConsumerThreads;
-    const uint32_t slot_bytes = (uint32_t)p.M * kTileCols * 4;
-    const int per_round = (int)((uint32_t)(kStages * kStageBytes) / slot_bytes);
-    const int units = p.M * kTileWords;   // (token, packed word) pairs of the tile
-    float sum[kUnits][8];
+    // Each thread owns float4 positions of the tile (pos = ctid + k * threads)
+    // and copies them from every contributor's partial into the idle stage
+    // ring with asynchronous 16-byte copies -- all in flight at once -- then
+    // adds them up in contributor order from its own slots (no barrier: a
+    // thread reads only what it copied). The order is fixed, so the result
+    // does not depend on timing. Only the first contributor may hold the
+    // tile in its second slot.
+    const int which_cf = (range_begin(cf, p.total, p.ctas) / p.kiters == t) ? 0 : 1;
+    constexpr int kPosPerThread = (kMaxTokens * kTileCols / 4 + kConsumerThreads - 1) / kConsumerThreads;
+    const int n4 = p.M * (kTileCols / 4);   // float4 positions of one partial
+    const int per_round = (kStages * kStageBytes) / (n4 * 16);
+    const uint32_t ring = ptx::smem_addr(smem);
+    float4 acc4[kPosPerThread];
 #pragma unroll
-    for (int q = 0; q < kUnits; ++q)
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) sum[q][jj] = 0.f;
-    bool ok = true;
-    for (int r0 = 0, round = 0; r0 < n; r0 += per_round, ++round) {
+    for (int k = 0; k < kPosPerThread; ++k) acc4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r0 = 0; r0 < n; r0 += per_round) {
         const int cnt = std::min(per_round, n - r0);
-        if (round > 0) ptx::named_barrier(1, kConsumerThreads);   // last round's reads are done
-        if (ctid == 0) {
-            // the partials were written through the generic proxy (and
-            // acquired above); the bulk copies read them through the async one
-            ptx::fence_proxy_async();
-            ptx::mbar_arrive_expect_tx(ptx::smem_addr(gather), (uint32_t)cnt * slot_bytes);
-            for (int q = 0; q < cnt; ++q) {
-                const int cc = cf + r0 + q;
-                const int which = (range_begin(cc, p.total, p.ctas) / p.kiters == t) ? 0 : 1;
-                ptx::bulk_load(ptx::smem_addr(smem + q * slot_bytes),
-                               p.partials + (int64_t)(2 * cc + which) * kPartialFloats, slot_bytes,
-                               ptx::smem_addr(gather));
+        for (int q = 0; q < cnt; ++q) {
+            const int ci = cf + r0 + q;
+            const float *slot = p.partials + (int64_t)(2 * ci + (ci == cf ? which_cf : 0)) * kPartialFloats;
+#pragma unroll
+            for (int k = 0; k < kPosPerThread; ++k) {
+                const int pos = ctid + k * kConsumerThreads;
+                if (pos < n4)
+                    ptx::cp_async_16(ring + (uint32_t)(q * n4 + pos) * 16,
+                                     slot + (pos / (kTileCols / 4)) * kTileCols + (pos % (kTileCols / 4)) * 4);
             }
         }
-        ok = ptx::mbar_wait_bounded(ptx::smem_addr(gather), (uint32_t)(round & 1), nullptr, p.status) && ok;
-        if (ok) {
+        ptx::cp_async_wait_all();
+        for (int q = 0; q < cnt; ++q) {
 #pragma unroll
-            for (int q = 0; q < kUnits; ++q) {
-                const int u = ctid + q * kConsumerThreads;
-                if (u < units) {
-                    const int m = u / kTileWords;
-                    const int w = u - m * kTileWords;
-                    const float *src = reinterpret_cast<const float *>(smem) + m * kTileCols + w * 8;
-                    for (int cc = 0; cc < cnt; ++cc) {
-                        const float4 lo = *reinterpret_cast<const float4 *>(src + cc * (slot_bytes / 4));
-                        const float4 hi = *reinterpret_cast<const float4 *>(src + cc * (slot_bytes / 4) + 4);
-                        sum[q][0] += lo.x; sum[q][1] += lo.y; sum[q][2] += lo.z; sum[q][3] += lo.w;
-                        sum[q][4] += hi.x; sum[q][5] += hi.y; sum[q][6] += hi.z; sum[q][7] += hi.w;
-                    }
+            for (int k = 0; k < kPosPerThread; ++k) {
+                const int pos = ctid + k * kConsumerThreads;
+                if (pos < n4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(smem + (size_t)(q * n4 + pos) * 16);
+                    acc4[k].x += v.x; acc4[k].y += v.y; acc4[k].z += v.z; acc4[k].w += v.w;
                 }
             }
         }
     }
-    if (ok && !*abort_flag) {
 #pragma unroll
-        for (int q = 0; q < kUnits; ++q) {
-            const int u = ctid + q * kConsumerThreads;
-            if (u >= units) continue;
-            const int m = u / kTileWords;
-            const int w = u - m * kTileWords;
-            const int col0 = t * kTileCols + w * 8;
-            if (col0 >= p.N) continue;
-            __align__(16) __half out[8];
-            if (p.bias) {
-                const uint4 braw = *reinterpret_cast<const uint4 *>(p.bias + col0);
-                const __half *bh = reinterpret_cast<const __half *>(&braw);
+    for (int k = 0; k < kPosPerThread; ++k) {
+        const int pos = ctid + k * kConsumerThreads;
+        if (pos >= n4) continue;
+        const int m = pos / (kTileCols / 4);
+        const int col = t * kTileCols + (pos % (kTileCols / 4)) * 4;
+        if (col >= p.N || *abort_flag) continue;
+        float b[4] = {0.f, 0.f, 0.f, 0.f};
+        if (p.bias) {
+            const uint2 braw = *reinterpret_cast<const uint2 *>(p.bias + col);
+            const __half *bh = reinterpret_cast<const __half *>(&braw);
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) out[jj] = __float2half_rn(sum[q][jj] + __half2float(bh[jj]));
-            } else {
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) out[jj] = __float2half_rn(sum[q][jj]);
-            }
-            *reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.N + col0) = *reinterpret_cast<const uint4 *>(out);
+            for (int jj = 0; jj < 4; ++jj) b[jj] = __half2float(bh[jj]);
         }
+        __align__(8) __half out[4] = {__float2half_rn(acc4[k].x + b[0]), __float2half_rn(acc4[k].y + b[1]),
+                                      __float2half_rn(acc4[k].z + b[2]), __float2half_rn(acc4[k].w + b[3])};
+        *reinterpret_cast<uint2 *>(p.y + (int64_t)m * p.N + col) = *reinterpret_cast<const uint2 *>(out);
     }
     // the counter is this CTA's alone now: reset it for the next call
     if (ctid == 0) atomicExch(p.arrive + t, 0u);

@@ -168,6 +168,16 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&d)[4]) {
                  : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]) : "r"(addr) : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only, not L1), and the wait
+// for every such copy this thread has issued.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Untiled bulk copy global -> shared (both 16-byte aligned, bytes % 16 == 0),
 // completion counted on `bar` in bytes.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
