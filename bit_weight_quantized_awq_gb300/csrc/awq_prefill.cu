@@ -12,20 +12,24 @@
 //   warp 0      TMA producer: per 64-deep k-stage, the x tile (128 x 64 fp16,
 //               K-major, 128-byte swizzle) and the packed-weight tile
 //               (64 k-rows x 32 words), plus the scale and zero-point rows of
-//               the groups the stage touches, into a 3-stage ring.
-//   warps 2-5   dequant: packed words -> fp16 W in shared memory, written
-//               directly in the MN-major 128-byte-swizzled layout the MMA reads
-//               as its B operand (one packed word = 8 consecutive columns =
-//               one 16-byte store). Per column pair: one byte permute puts the
-//               word's byte p in both halves, one LOP3 masks the low nibble
-//               into the fraction of 1024.0 and the high nibble into that of
-//               64.0, one half2 subtract removes (1024 + z, 64 + z) exactly,
-//               one half2 multiply by the (s, s') pair -- which is simply the
-//               scales word -- rounds once: exactly fp16_rn((q - z) s).
+//               the groups the stage touches, into a 5-stage ring (only what
+//               comes from global memory sits in the ring, so it can be deep
+//               enough to cover the load latency).
+//   warps 2-9   dequant: packed words -> fp16 W in one of two B slots,
+//               written directly in the MN-major 128-byte-swizzled layout the
+//               MMA reads as its B operand (one packed word = 8 columns = one
+//               16-byte store). Per column pair (c, c + 4) of a word: one LOP3
+//               masks the two nibbles into the fraction of 1024.0 (low nibble
+//               of a byte) or 64.0 (high nibble), one half2 subtract removes
+//               (1024 + z) or (64 + z) exactly, one half2 multiply by the
+//               scales rounds once: exactly fp16_rn((q - z) s). The columns of
+//               every group of 8 are therefore stored as 0 4 1 5 2 6 3 7, and
+//               the epilogue undoes that order.
 //   warp 1      MMA issuer (one thread) and TMEM owner: 4 MMAs per stage into
 //               one of two 256-column fp32 accumulators, tcgen05.commit frees
-//               the stage and, at the last stage, hands the accumulator over.
-//   warps 6-9   epilogue: tcgen05.ld of the accumulator (each warp its 32
+//               the stage and the B slot and, at the last stage, hands the
+//               accumulator over.
+//   warps 10-13 epilogue: tcgen05.ld of the accumulator (each warp its 32
 //               lanes = 32 tokens), + bias, one rounding to fp16, store. With
 //               two accumulators the epilogue of one tile overlaps the
 //               main loop of the next.
@@ -57,36 +61,53 @@ namespace {
 constexpr int BM = 128;          // tokens per tile (MMA M)
 constexpr int BN = 256;          // output columns per tile (MMA N)
 constexpr int BK = 64;           // k per stage (one 128-byte swizzle row of fp16)
-constexpr int kStages = 3;
 constexpr int kMmaK = 16;
 constexpr int kMaxGroupRows = 5;
 
 constexpr int kABytes = BM * BK * 2;            // 16 KB
 constexpr int kBBytes = BN * BK * 2;            // 32 KB
 constexpr int kPBytes = BK * (BN / 8) * 4;      // 8 KB
-constexpr int kSBytes = kMaxGroupRows * BN * 2;
-constexpr int kZBytes = kMaxGroupRows * (BN / 8) * 4;
-constexpr int kAOff = 0;
-constexpr int kBOff = kAOff + kABytes;
-constexpr int kPOff = kBOff + kBBytes;
-constexpr int kSOff = kPOff + kPBytes;
-constexpr int kZOff = kSOff + kSBytes;
-constexpr int kStageBytes = 60 * 1024;
-static_assert(kZOff + kZBytes <= kStageBytes, "stage layout overflows");
-static_assert(kStageBytes % 1024 == 0 && kBOff % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-constexpr int kBarOff = kStages * kStageBytes;
-constexpr int kSmemBytes = kBarOff + 256 + 1024;
+
+// Shared memory. With dequantisation the TMA ring carries only what comes
+// from global memory -- the x tile, the packed-weight tile and the scale and
+// zero-point rows (28 KB a stage, five stages, enough to cover the load
+// latency) -- and the dequantised B tiles the MMA reads live in a separate
+// pair of slots that the dequant warps fill. Without dequantisation
+// (awq_gemm_f16) a stage is the x tile plus the fp16 B tile, four stages.
+template <bool kDequant>
+struct Cfg {
+    static constexpr int kStages = kDequant ? 5 : 4;
+    static constexpr int kAOff = 0;
+    static constexpr int kPOff = kABytes;                       // packed words (dequant)
+    static constexpr int kSOff = kPOff + kPBytes;               // scale rows (dequant)
+    static constexpr int kZOff = kSOff + kMaxGroupRows * BN * 2; // zero-point rows (dequant)
+    static constexpr int kStageBytes = kDequant ? 28 * 1024 : kABytes + kBBytes;
+    static constexpr int kBSlots = kDequant ? 2 : 0;
+    static constexpr int kBSlotOff = kStages * kStageBytes;
+    static constexpr int kBarOff = kBSlotOff + kBSlots * kBBytes;
+    static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+    static_assert(!kDequant || kZOff + kMaxGroupRows * (BN / 8) * 4 <= kStageBytes, "stage layout overflows");
+    static_assert(kStageBytes % 1024 == 0 && kBSlotOff % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
 
 // B tile layout (MN-major, 128-byte swizzle): 4 column atoms of 64 columns,
 // each 8 k-groups of (8 k-rows x 128 bytes).
 constexpr int kBAtomStride = 8 * 1024;   // between 64-column atoms (leading byte offset)
 constexpr int kBKGroupStride = 1024;     // between 8-row k groups (stride byte offset)
 
-constexpr int kWarps = 10;
+// Inside every 8-column group the dequantised tile stores the columns in the
+// order 0 4 1 5 2 6 3 7 (one LOP3 yields columns c and c + 4 of a packed word
+// without a byte permute); the accumulator columns come out in that order
+// and the epilogue puts them back: output column q of a group is accumulator
+// column unperm(q).
+__host__ __device__ constexpr int unperm(int q) { return q < 4 ? 2 * q : 2 * (q - 4) + 1; }
+
+constexpr int kWarps = 14;
 constexpr int kThreads = kWarps * 32;
 constexpr int kDequantWarp0 = 2;
-constexpr int kEpilogueWarp0 = 6;
-constexpr int kDequantThreads = 128;
+constexpr int kEpilogueWarp0 = 10;
+constexpr int kDequantThreads = 256;
 constexpr int kEpilogueThreads = 128;
 constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
 
@@ -110,21 +131,57 @@ __device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
     return *reinterpret_cast<uint32_t *>(&r);
 }
 
-template <bool kDequant>
+// Scales and zero points of one group for packed word j, in the register
+// order of the dequantised columns: pair q holds columns (q, q + 4).
+__device__ __forceinline__ void load_group(uint32_t s_row, uint32_t z_row, uint32_t (&S)[4], uint32_t (&Z)[4])
+{
+    uint32_t sv0, sv1, sv2, sv3, zw;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(sv0), "=r"(sv1), "=r"(sv2), "=r"(sv3) : "r"(s_row));
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(zw) : "r"(z_row));
+    S[0] = __byte_perm(sv0, sv2, 0x5410);   // (s0, s4)
+    S[1] = __byte_perm(sv0, sv2, 0x7632);   // (s1, s5)
+    S[2] = __byte_perm(sv1, sv3, 0x5410);   // (s2, s6)
+    S[3] = __byte_perm(sv1, sv3, 0x7632);   // (s3, s7)
+    const uint32_t zh = zw >> 8;
+    Z[0] = (zw & 0x000F000Fu) | 0x64006400u;   // 1024 + (z0, z4)
+    Z[1] = (zw & 0x00F000F0u) | 0x54005400u;   // 64 + (z1, z5)
+    Z[2] = (zh & 0x000F000Fu) | 0x64006400u;   // 1024 + (z2, z6)
+    Z[3] = (zh & 0x00F000F0u) | 0x54005400u;   // 64 + (z3, z7)
+}
+
+// One packed word (8 columns of one k-row) -> four half2 registers of
+// fp16_rn((q - z) s): the nibble ORed into the fraction of 1024.0 (low
+// nibble of a byte) or 64.0 (high nibble, one sixteenth per unit), an exact
+// subtraction of (1024 + z) or (64 + z), one multiply rounding once.
+__device__ __forceinline__ void dequant_word(uint32_t v, const uint32_t (&S)[4], const uint32_t (&Z)[4],
+                                             uint32_t (&h)[4])
+{
+    const uint32_t vh = v >> 8;
+    h[0] = hmul2_u(hsub2_u((v & 0x000F000Fu) | 0x64006400u, Z[0]), S[0]);
+    h[1] = hmul2_u(hsub2_u((v & 0x00F000F0u) | 0x54005400u, Z[1]), S[1]);
+    h[2] = hmul2_u(hsub2_u((vh & 0x000F000Fu) | 0x64006400u, Z[2]), S[2]);
+    h[3] = hmul2_u(hsub2_u((vh & 0x00F000F0u) | 0x54005400u, Z[3]), S[3]);
+}
+
+template <bool kDequant, bool kWhole>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
                const PrefillParams p)
 {
+    using C = Cfg<kDequant>;
+    constexpr int kStages = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     // round up to 1024 bytes by offsetting the shared array itself, so that
     // the compiler still knows every derived pointer is a shared address
     uint8_t *smem = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kBarOff);
-    uint64_t *dqd = full + kStages;        // dequantised B ready
-    uint64_t *empty = dqd + kStages;       // MMAs of the stage done
-    uint64_t *acc_full = empty + kStages;  // [2]
-    uint64_t *acc_empty = acc_full + 2;    // [2]
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);   // [kStages] TMA bytes landed
+    uint64_t *tfree = full + kStages;       // [kStages] MMAs that read the stage are done
+    uint64_t *bready = tfree + kStages;     // [2] dequantised B slot written
+    uint64_t *bfree = bready + 2;           // [2] MMAs that read the B slot are done
+    uint64_t *acc_full = bfree + 2;         // [2]
+    uint64_t *acc_empty = acc_full + 2;     // [2]
     uint64_t *drain = acc_empty + 2;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -136,10 +193,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(ptx::smem_addr(full + s), 1);
-            ptx::mbar_init(ptx::smem_addr(dqd + s), kDequantThreads);
-            ptx::mbar_init(ptx::smem_addr(empty + s), 1);
+            ptx::mbar_init(ptx::smem_addr(tfree + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(ptx::smem_addr(bready + b), kDequantThreads);
+            ptx::mbar_init(ptx::smem_addr(bfree + b), 1);
             ptx::mbar_init(ptx::smem_addr(acc_full + b), 1);
             ptx::mbar_init(ptx::smem_addr(acc_empty + b), kEpilogueThreads);
         }
@@ -172,24 +230,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 const int n0 = (tile / p.tiles_m) * BN;
                 for (int kb = 0; kb < p.kiters; ++kb, ++it) {
                     const int s = it % kStages;
-                    if (!ptx::mbar_wait_bounded(ptx::smem_addr(empty + s), ((it / kStages) & 1) ^ 1,
+                    if (!ptx::mbar_wait_bounded(ptx::smem_addr(tfree + s), ((it / kStages) & 1) ^ 1,
                                                 abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = ptx::smem_addr(full + s);
-                    const uint32_t st = ptx::smem_addr(smem + s * kStageBytes);
+                    const uint32_t st = ptx::smem_addr(smem + s * C::kStageBytes);
                     const int k0 = kb * BK;
                     ptx::mbar_arrive_expect_tx(fb, p.stage_tx);
-                    ptx::tma_load_2d(st + kAOff, &tm_x, fb, k0, m0);
+                    ptx::tma_load_2d(st + C::kAOff, &tm_x, fb, k0, m0);
                     if (kDequant) {
-                        ptx::tma_load_2d(st + kPOff, &tm_w, fb, n0 / 8, k0);
-                        ptx::tma_load_2d(st + kSOff, &tm_s, fb, n0, k0 / p.g);
-                        ptx::tma_load_2d(st + kZOff, &tm_z, fb, n0 / 8, k0 / p.g);
+                        ptx::tma_load_2d(st + C::kPOff, &tm_w, fb, n0 / 8, k0);
+                        ptx::tma_load_2d(st + C::kSOff, &tm_s, fb, n0, k0 / p.g);
+                        ptx::tma_load_2d(st + C::kZOff, &tm_z, fb, n0 / 8, k0 / p.g);
                     } else {
 #pragma unroll
                         for (int a = 0; a < BN / 64; ++a)
-                            ptx::tma_load_2d(st + kBOff + a * kBAtomStride, &tm_w, fb, n0 + 64 * a, k0);
+                            ptx::tma_load_2d(st + kABytes + a * kBAtomStride, &tm_w, fb, n0 + 64 * a, k0);
                     }
                     issued = it + 1;
                 }
@@ -217,24 +275,29 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 const uint32_t d_tmem = tmem_base + (uint32_t)(abuf * BN);
                 for (int kb = 0; kb < p.kiters; ++kb, ++it) {
                     const int s = it % kStages;
-                    const uint32_t par = (it / kStages) & 1;
-                    bool ready = ptx::mbar_wait_bounded(ptx::smem_addr(full + s), par, abort_flag, p.status);
+                    const int b = it & 1;
+                    bool ready = ptx::mbar_wait_bounded(ptx::smem_addr(full + s), (it / kStages) & 1,
+                                                        abort_flag, p.status);
                     if (ready && kDequant)
-                        ready = ptx::mbar_wait_bounded(ptx::smem_addr(dqd + s), par, abort_flag, p.status);
+                        ready = ptx::mbar_wait_bounded(ptx::smem_addr(bready + b), (it >> 1) & 1,
+                                                       abort_flag, p.status);
                     if (!ready) {
                         ok = false;
                         break;
                     }
                     tc::fence_after_sync();
-                    const uint32_t st = ptx::smem_addr(smem + s * kStageBytes);
+                    const uint32_t st = ptx::smem_addr(smem + s * C::kStageBytes);
+                    const uint32_t bt = kDequant ? ptx::smem_addr(smem + C::kBSlotOff + b * kBBytes)
+                                                 : st + kABytes;
 #pragma unroll
                     for (int kk = 0; kk < BK / kMmaK; ++kk) {
-                        const uint64_t ad = tc::smem_desc_sw128(st + kAOff + kk * 32, 16, 1024);
-                        const uint64_t bd = tc::smem_desc_sw128(st + kBOff + kk * 2 * kBKGroupStride,
+                        const uint64_t ad = tc::smem_desc_sw128(st + C::kAOff + kk * 32, 16, 1024);
+                        const uint64_t bd = tc::smem_desc_sw128(bt + kk * 2 * kBKGroupStride,
                                                                 kBAtomStride, kBKGroupStride);
                         tc::mma_f16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
                     }
-                    tc::commit(ptx::smem_addr(empty + s));
+                    tc::commit(ptx::smem_addr(tfree + s));
+                    if (kDequant) tc::commit(ptx::smem_addr(bfree + b));
                     if (kb == p.kiters - 1) tc::commit(ptx::smem_addr(acc_full + abuf));
                 }
             }
@@ -245,62 +308,66 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     } else if (warp < kEpilogueWarp0) {
         // ------------------------------------------------------------ dequant
         if (kDequant) {
-            const int dt = threadIdx.x - kDequantWarp0 * 32;   // 0..127
-            const int dw = dt >> 5;                            // row phase 0..3
-            const int j = dt & 31;                             // packed word in the tile row
-            const int na = j >> 3, chunk = j & 7;
+            const int dt = threadIdx.x - kDequantWarp0 * 32;   // 0..255
+            const int dw = dt >> 5;            // k-row inside every 8-row group: dw, dw + 8, ...
+            const int j = dt & 31;             // packed word (8 columns) in the tile row
+            // B slot: 64-column atom j / 8, 16-byte chunk (j % 8) ^ row in the
+            // 128-byte swizzle; the k-group adds 1024 bytes
+            const uint32_t b_in = (uint32_t)(j >> 3) * kBAtomStride + (uint32_t)dw * 128 +
+                                  ((uint32_t)((j & 7) ^ dw) << 4);
+            const uint32_t p_in = C::kPOff + (uint32_t)dw * 128 + (uint32_t)j * 4;
+            const uint32_t s_in = C::kSOff + (uint32_t)j * 16;
+            const uint32_t z_in = C::kZOff + (uint32_t)j * 4;
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
                 for (int kb = 0; kb < p.kiters; ++kb, ++it) {
                     const int s = it % kStages;
-                    if (!ptx::mbar_wait_bounded(ptx::smem_addr(full + s), (it / kStages) & 1,
-                                                abort_flag, p.status)) {
+                    const int b = it & 1;
+                    bool ready = ptx::mbar_wait_bounded(ptx::smem_addr(full + s), (it / kStages) & 1,
+                                                        abort_flag, p.status);
+                    if (ready)
+                        ready = ptx::mbar_wait_bounded(ptx::smem_addr(bfree + b), ((it >> 1) & 1) ^ 1,
+                                                       abort_flag, p.status);
+                    if (!ready) {
                         ok = false;
                         break;
                     }
-                    const uint32_t st = ptx::smem_addr(smem + s * kStageBytes);
-                    const uint32_t pbase = st + kPOff + j * 4;
-                    const uint32_t bbase = st + kBOff + na * kBAtomStride;
-                    const int k0 = kb * BK;
-                    const int grp0 = k0 / p.g;
-                    int cur = -1;
+                    const uint32_t st = ptx::smem_addr(smem + s * C::kStageBytes);
+                    const uint32_t bb = ptx::smem_addr(smem + C::kBSlotOff + b * kBBytes) + b_in;
                     uint32_t S[4], Z[4];
-#pragma unroll 4
-                    for (int i = 0; i < BK / 4; ++i) {
-                        const int row = dw + 4 * i;
-                        const int grp = (k0 + row) / p.g;
-                        if (grp != cur) {
-                            cur = grp;
-                            const int r = grp - grp0;
-                            uint32_t sv0, sv1, sv2, sv3, zw;
-                            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                         : "=r"(sv0), "=r"(sv1), "=r"(sv2), "=r"(sv3)
-                                         : "r"(st + kSOff + r * (BN * 2) + j * 16));
-                            asm volatile("ld.shared.b32 %0, [%1];"
-                                         : "=r"(zw) : "r"(st + kZOff + r * (BN / 8 * 4) + j * 4));
-                            S[0] = sv0; S[1] = sv1; S[2] = sv2; S[3] = sv3;
+                    int r = 0, rem = 0;
+                    if (kWhole) {
+                        // g % 64 == 0: the whole stage lies in one group
+                        load_group(st + s_in, st + z_in, S, Z);
+                    } else {
+                        const int k0 = kb * BK;
+                        const int grp0 = k0 / p.g;
+                        r = (k0 + dw) / p.g - grp0;   // group row of this thread's first k-row
+                        rem = (k0 + dw) - (r + grp0) * p.g;
+                        load_group(st + s_in + r * (BN * 2), st + z_in + r * (BN / 8 * 4), S, Z);
+                    }
 #pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                Z[q] = (__byte_perm(zw, zw, q | (q << 8)) & 0x00F0000Fu) | 0x54006400u;
+                    for (int i = 0; i < BK / 8; ++i) {
+                        if (!kWhole && i > 0) {
+                            rem += 8;   // g >= 16: at most one group boundary per step
+                            if (rem >= p.g) {
+                                rem -= p.g;
+                                ++r;
+                                load_group(st + s_in + r * (BN * 2), st + z_in + r * (BN / 8 * 4), S, Z);
+                            }
                         }
                         uint32_t v;
-                        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(pbase + row * 128));
+                        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(st + p_in + i * 1024));
                         uint32_t h[4];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const uint32_t w = (__byte_perm(v, v, q | (q << 8)) & 0x00F0000Fu) | 0x54006400u;
-                            h[q] = hmul2_u(hsub2_u(w, Z[q]), S[q]);
-                        }
-                        const int krow = row & 7;
-                        const uint32_t dst = bbase + (row >> 3) * kBKGroupStride + krow * 128 +
-                                             (((uint32_t)chunk ^ (uint32_t)krow) << 4);
+                        dequant_word(v, S, Z, h);
                         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                                     ::"r"(dst), "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]) : "memory");
+                                     ::"r"(bb + i * kBKGroupStride), "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                                     : "memory");
                     }
                     // make the generic-proxy stores visible to the tensor core
                     ptx::fence_proxy_async_smem();
-                    ptx::mbar_arrive(ptx::smem_addr(dqd + s));
+                    ptx::mbar_arrive(ptx::smem_addr(bready + b));
                 }
             }
         }
@@ -320,9 +387,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             const int m = m0 + 32 * q + lane;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tc::ld_32x32b_x32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(abuf * BN + 32 * c), r);
+                uint32_t raw[32];
+                tc::ld_32x32b_x32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(abuf * BN + 32 * c), raw);
                 tc::ld_wait();
+                uint32_t r[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] = kDequant ? raw[(e & ~7) + unperm(e & 7)] : raw[e];
                 const int col = n0 + 32 * c;
                 if (col < p.N && m < p.M) {
                     __align__(16) __half out[32];
@@ -401,7 +471,7 @@ struct LaunchInfo {
     cudaError_t err = cudaSuccess;
 };
 
-template <bool kDequant>
+template <bool kDequant, bool kWhole>
 LaunchInfo launch_info()
 {
     static std::mutex mu;
@@ -413,18 +483,18 @@ LaunchInfo launch_info()
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(dev);
     if (it != cache.end()) return it->second;
-    li.err = cudaFuncSetAttribute(prefill_kernel<kDequant>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  kSmemBytes);
+    li.err = cudaFuncSetAttribute(prefill_kernel<kDequant, kWhole>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  Cfg<kDequant>::kSmemBytes);
     if (li.err == cudaSuccess)
         li.err = cudaDeviceGetAttribute(&li.sms, cudaDevAttrMultiProcessorCount, dev);
     if (li.err == cudaSuccess) cache[dev] = li;
     return li;
 }
 
-template <bool kDequant>
+template <bool kDequant, bool kWhole>
 cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream)
 {
-    const LaunchInfo li = launch_info<kDequant>();
+    const LaunchInfo li = launch_info<kDequant, kWhole>();
     if (li.err != cudaSuccess) return li.err;
     const int M = (int)pr.M, K = (int)pr.K, N = (int)pr.N, g = (int)pr.g;
     const int tiles_m = (M + BM - 1) / BM;
@@ -463,7 +533,7 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream)
     p.M = M; p.K = K; p.N = N; p.g = g;
     p.tiles_m = tiles_m; p.tiles_n = tiles_n; p.kiters = kiters;
     p.stage_tx = tx_bytes;
-    prefill_kernel<kDequant><<<ctas, kThreads, kSmemBytes, stream>>>(tx, tw, ts, tz, p);
+    prefill_kernel<kDequant, kWhole><<<ctas, kThreads, Cfg<kDequant>::kSmemBytes, stream>>>(tx, tw, ts, tz, p);
     return cudaGetLastError();
 }
 
@@ -478,12 +548,13 @@ bool prefill_supported(int64_t M, int64_t K, int64_t N, int64_t g)
 cudaError_t launch_prefill(const Problem &p, cudaStream_t stream)
 {
     if (!prefill_supported(p.M, p.K, p.N, p.g)) return cudaErrorInvalidValue;
-    return launch<true>(p, nullptr, stream);
+    // g % 64 == 0: every 64-row stage lies in one group
+    return p.g % BK == 0 ? launch<true, true>(p, nullptr, stream) : launch<true, false>(p, nullptr, stream);
 }
 
 cudaError_t launch_gemm_f16(const Problem &p, const void *w16, cudaStream_t stream)
 {
-    return launch<false>(p, w16, stream);
+    return launch<false, true>(p, w16, stream);
 }
 
 } // namespace awq
