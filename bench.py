@@ -40,6 +40,39 @@ if ROOT not in sys.path:
 
 METRIC = "AWQ W4A16 GEMM TFLOP/s and weight GB/s vs M (1..8192), % of roofline, 1xGB300"
 
+# DRAM bytes per launch of the dominant kernel, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum, mean over one step's
+# launches), valid only while the kernel sources hash to what was captured.
+NCU_TRAFFIC = {
+    "decode-7b": {
+        "bytes_per_launch": 26405909,
+        "sources": {
+            "bit_weight_quantized_awq_gb300/csrc/awq_decode.cu":
+                "047c5c9b6a0b255bba3da8e0118fe6069d4f92cb2c949d9963afe95db01e5b9e",
+            "bit_weight_quantized_awq_gb300/csrc/awq_device.cuh":
+                "0d6b8739c00fe7c14482c2d22a020cbabd9e60a7b0dad4bc1f07068019c49aa4",
+        },
+        "summary": "profiles/decode_kernel_decode-7b.md",
+    },
+}
+
+
+def ncu_traffic(workload):
+    """(bytes per launch, note) of the committed capture, or (None, why)."""
+    import hashlib
+    rec = NCU_TRAFFIC.get(workload)
+    if rec is None:
+        return None, "no ncu capture of this workload"
+    root = os.path.dirname(os.path.abspath(__file__))
+    for rel, digest in rec["sources"].items():
+        try:
+            with open(os.path.join(root, rel), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None, f"{rel} changed since the capture"
+        except OSError:
+            return None, f"{rel} not readable"
+    return rec["bytes_per_launch"], rec["summary"]
+
 DECODE_SHAPES = [(4096, 4096), (4096, 12288), (4096, 22016), (11008, 4096)]
 PREFILL_SHAPES = [(4096, 12288), (4096, 22016), (11008, 4096)]
 SWEEP_SHAPES = [(8192, 10240), (8192, 57344), (28672, 8192)]
@@ -537,13 +570,26 @@ def main():
         # duration is the timed region over the launches in it
         launch_s = r["elapsed"] / (args.steps * len(problems))
         achieved = r["abytes"] / len(problems) / launch_s / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": None,
-                "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
-                "kernel": names.get(dominant, "?"),
-                "bytes_per_launch_avg": r["abytes"] / len(problems),
-                "launch_us_avg": launch_s * 1e6,
-                "how": "algorithmic bytes per launch / (timed region / launches), back-to-back graph replays"}
+        traffic, traffic_note = ncu_traffic(args.workload)
+        if dominant == 3:
+            # the tcgen05 contraction: fp16 operands, whose nominal dense rate
+            # equals bf16's, so the measured bf16 cuBLAS peak is the roof
+            tf = r["flops"] / len(problems) / launch_s / 1e12
+            roof = {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": tf / peaks["bf16_tflops"], "traffic": traffic, "traffic_source": traffic_note,
+                    "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json bf16_tflops, burst; fp16 = bf16 nominal)",
+                    "kernel": names.get(dominant, "?"),
+                    "flops_per_launch_avg": r["flops"] / len(problems),
+                    "launch_us_avg": launch_s * 1e6,
+                    "how": "algorithmic flops per launch / (timed region / launches), back-to-back graph replays"}
+        else:
+            roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "traffic_source": traffic_note,
+                    "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
+                    "kernel": names.get(dominant, "?"),
+                    "bytes_per_launch_avg": r["abytes"] / len(problems),
+                    "launch_us_avg": launch_s * 1e6,
+                    "how": "algorithmic bytes per launch / (timed region / launches), back-to-back graph replays"}
     if r["per_problem"]:
         avg = [statistics.mean(ts) for ts in r["per_problem"]]
         per = [{"M": p[0], "K": p[1], "N": p[2], "us_isolated": round(a * 1e6, 3),
