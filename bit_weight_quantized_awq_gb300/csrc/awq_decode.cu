@@ -7,27 +7,35 @@
 // At small M the layer is bound by streaming the packed weights from HBM
 // (0.52 bytes per weight at g = 128). The kernel is built around that:
 //
-//  * Work: the K x N weight matrix is cut into tiles of 256 columns (one
-//    128-byte row of packed words) and stages of 256 k-rows. The (tile,
-//    stage) iterations, tile-major, are split evenly between the CTAs (one
-//    per SM): each CTA streams a contiguous run of them ("stream-K").
-//  * Loads: one producer warp issues four TMA boxes per stage -- 256 x 128 B
-//    of qweight (32 KB, 128-byte swizzle), the 256 x Mpad activation slice
-//    (one 3-D box), and the scale and zero-point rows of the groups the stage
-//    touches -- into a 4-stage ring guarded by mbarriers (full: bytes landed;
-//    empty: the consumers released the slot). Issuing a TMA instruction costs
-//    the producer on the order of a hundred cycles, so each one moves as many
-//    bytes as the box limits allow.
-//  * Math: 8 consumer warps: two k-groups (group kg takes rows 128 kg ..
-//    128 kg + 127 of every stage, eight 16-row chunks) of four warps (each
-//    owns 64 columns). Each warp dequantises in registers and runs the legacy-path
-//    tensor-core MMA m16n8k16 with W as the A operand (16 output columns x 16
-//    k) and the activations as B (16 k x 8 tokens), fp32 accumulators. Two
-//    k-adjacent weights of one column form one half2 operand register: a byte
-//    permute brings byte b of rows k and k+1 together, one LOP3 masks a nibble
-//    into the fraction of 1024.0 or 64.0, an exact half2 subtract removes the
-//    zero point and one half2 multiply (round to nearest) applies the scale --
-//    exactly fp16_rn((q - z) s).
+//  * Work: the K x N weight matrix is cut into column tiles of CW 128-byte
+//    chunks of packed words (CW = 1: 256 columns; CW = 2: 512 columns, used
+//    when N is a multiple of 512 and at least 8192) and stages of 32 KB of
+//    packed weights (256 / CW k-rows). The (tile, stage) iterations,
+//    tile-major, are split evenly between the CTAs (one per SM): each CTA
+//    streams a contiguous run of them ("stream-K"). Rows 256 bytes wide keep
+//    HBM reads of large matrices ~20 % closer to the copy bandwidth than
+//    128-byte rows; on small N the narrower tile keeps split-K short.
+//  * Loads: thread 0 issues four TMA boxes per stage -- the qweight slice
+//    (32 KB, 128-byte swizzle), the activation slice (one 3-D box), and the
+//    scale and zero-point rows of the groups the stage touches -- into a ring
+//    of as many stages as shared memory holds (5-6 at g = 128), guarded by
+//    mbarriers (full: bytes landed; empty: every warp released the slot).
+//    All but one slot are in flight ahead of the stage being computed; after
+//    each stage thread 0 refills the slot released one stage earlier, so it
+//    seldom waits. Issuing a TMA instruction costs on the order of a hundred
+//    cycles, so each one moves as many bytes as the box limits allow.
+//  * Math: 16 warps, each taking 64 rows x 64 columns of every stage (four
+//    16-row chunks): 4 / CW k-groups of 4 CW column warps. Each warp
+//    dequantises in registers and runs the legacy-path tensor-core MMA
+//    m16n8k16 with W as the A operand (16 output columns x 16 k) and the
+//    activations as B (16 k x 8 tokens), fp32 accumulators. Two k-adjacent
+//    weights of one column form one half2 operand register: a byte permute
+//    brings byte b of rows k and k+1 together, one LOP3 masks a nibble into
+//    the fraction of 1024.0 or 64.0, an exact half2 subtract removes the zero
+//    point and one half2 multiply (round to nearest) applies the scale --
+//    exactly fp16_rn((q - z) s). At the end of a tile's run the k-groups are
+//    summed in a fixed order through the weight area of the slot just
+//    consumed, which is released afterwards.
 //  * Reduction: a tile split between CTAs is finished by the CTA that holds
 //    its last k-stages, which is the highest-numbered contributor (its range
 //    starts inside the tile). Every contributor writes its fp32 partial to
@@ -56,55 +64,46 @@
 namespace awq {
 namespace {
 
-constexpr int kTileWords = 32;   // packed words per tile row
-constexpr int kTileCols = 256;   // output columns per tile
-constexpr int kStageRows = 256;  // k-rows per pipeline stage
-constexpr int kStages = 4;
-constexpr int kKBlocks = kStageRows / 64;   // 64-row blocks of a stage (activation layout)
-constexpr int kColWarps = 4;     // warps across a tile's columns, 8 words each
-
-// Warp layout for KG consumer k-groups: k-group kg takes stage rows
-// kRowsPerWarp * kg .. + kRowsPerWarp - 1, split in 16-row chunks; each of its
-// kColWarps warps owns 64 columns. One producer warp follows the consumers.
-template <int KG>
-struct Layout {
-    static constexpr int kKGroups = KG;
-    static constexpr int kRowsPerWarp = kStageRows / KG;
-    static constexpr int kChunksPerWarp = kRowsPerWarp / 16;
-    static constexpr int kConsumerWarps = kColWarps * KG;
-    static constexpr int kConsumerThreads = kConsumerWarps * 32;
-    static constexpr int kThreads = kConsumerThreads + 32;
-};
 constexpr int kMaxTokens = 16;
-constexpr int kMaxGroupRows = 8; // group rows one stage may touch (g >= 32)
+constexpr int kMaxGroupRows = 8;     // group rows one stage may touch
+constexpr int kWBytes = 32768;       // packed weights per stage
+constexpr int kMaxStages = 8;
+constexpr int kConsumerWarps = 8;    // dequantise + MMA
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;   // + one TMA producer warp
+constexpr int kBarBytes = 2 * kMaxStages * 8 + 64;   // full/empty barriers + flags
+constexpr int kSmemLimit = 227 * 1024;
+constexpr int kMaxTileCols = 512;
+constexpr int kMaxPartialFloats = kMaxTokens * kMaxTileCols;  // one partial slot
 
-constexpr int kWBytes = kStageRows * 128;
-constexpr int kXBytes = kMaxTokens * kStageRows * 2;
-constexpr int kSBytes = kMaxGroupRows * kTileCols * 2;
-constexpr int kZBytes = kMaxGroupRows * kTileWords * 4;
-constexpr int kXOff = kWBytes;
-constexpr int kSOff = kXOff + kXBytes;
-constexpr int kZOff = kSOff + kSBytes;
-constexpr int kStageBytes = 45 * 1024;
-static_assert(kZOff + kZBytes <= kStageBytes, "stage layout overflows");
-static_assert(kStageBytes % 1024 == 0 && kXOff % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-constexpr int kFoldFloats = kMaxTokens * kTileCols;     // one k-group's sums
-constexpr int kRedOff = kStages * kStageBytes;
-constexpr int kRedBytes = 2 * kFoldFloats * 4;
-constexpr int kBarOff = kRedOff + kRedBytes;
-constexpr int kSmemBytes = kBarOff + 256 + 1024;   // barriers + flags + alignment slack
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-
-constexpr int kPartialFloats = kMaxTokens * kTileCols;  // one partial slot
+// Tile geometry for CW 128-byte chunks of packed words per weight row.
+template <int CW>
+struct Geo {
+    static constexpr int kTileWords = 32 * CW;
+    static constexpr int kTileCols = 256 * CW;
+    static constexpr int kStageRows = kWBytes / (kTileWords * 4);
+    static constexpr int kKBlocks = kStageRows / 64;     // 64-row blocks of a stage
+    static constexpr int kColWarps = 4 * CW;                      // warps across a tile (64 columns each)
+    static constexpr int kKGroups = kConsumerWarps / kColWarps;   // warps down a stage
+    static constexpr int kRowsPerWarp = kStageRows / kKGroups;    // 128
+    static constexpr int kChunksPerWarp = kRowsPerWarp / 16;
+    static constexpr int kPartialFloats = kMaxTokens * kTileCols;   // also one k-group's fold
+    static_assert(kKGroups * kRowsPerWarp == kStageRows, "warps must cover a stage");
+};
+static_assert(Geo<1>::kKGroups == 2 && Geo<1>::kPartialFloats * 4 <= kWBytes, "CW = 1 folds one k-group");
+static_assert(Geo<2>::kKGroups == 1, "CW = 2 has nothing to fold");
 
 struct DecodeParams {
     const __half *bias;
     __half *y;
-    float *partials;        // [2 * ctas][16][256]
+    float *partials;        // [2 * ctas][16][tile columns]
     unsigned int *arrive;   // [tiles]
     unsigned int *status;
     int M, K, N, g;
     int tiles, kiters, total, ctas;
+    int stages;             // ring slots
+    uint32_t stage_bytes;   // bytes per slot (multiple of 1024)
+    uint32_t x_off, s_off, z_off;  // activation / scale / zero rows inside a slot
     uint32_t stage_tx;      // bytes one stage's TMA boxes deliver
 };
 
@@ -126,47 +125,57 @@ __device__ __forceinline__ int range_begin(int c, int total, int ctas) {
     return (int)(((int64_t)c * total) / ctas);
 }
 
-template <int MT>
+// One k-group's accumulators to / from shared memory; STRIDE = threads of a
+// k-group, so that consecutive threads touch consecutive words.
+template <int MT, int STRIDE>
 __device__ __forceinline__ void fold_store(float *dst, const float (&acc)[4][MT][4], int ct) {
 #pragma unroll
     for (int b = 0; b < 4; ++b)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) dst[((b * MT + mt) * 4 + e) * 128 + ct] = acc[b][mt][e];
+            for (int e = 0; e < 4; ++e) dst[((b * MT + mt) * 4 + e) * STRIDE + ct] = acc[b][mt][e];
 }
-template <int MT>
+template <int MT, int STRIDE>
 __device__ __forceinline__ void fold_add(const float *src, float (&acc)[4][MT][4], int ct) {
 #pragma unroll
     for (int b = 0; b < 4; ++b)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[b][mt][e] += src[((b * MT + mt) * 4 + e) * 128 + ct];
+            for (int e = 0; e < 4; ++e) acc[b][mt][e] += src[((b * MT + mt) * 4 + e) * STRIDE + ct];
 }
 
-template <int MT, int KG, bool kWholeGroups>
-__global__ void __launch_bounds__(Layout<KG>::kThreads, 1)
+template <int MT, int CW, bool kWholeGroups>
+__global__ void __launch_bounds__(kThreads, 1)
 decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
               const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
               const DecodeParams p)
 {
+    using G = Geo<CW>;
+    constexpr int kTileCols = G::kTileCols;
+    constexpr int kTileWords = G::kTileWords;
+    constexpr int kStageRows = G::kStageRows;
+    constexpr int kKBlocks = G::kKBlocks;
+    constexpr int kColWarps = G::kColWarps;
+    constexpr int KG = G::kKGroups;
+    constexpr int kChunksPerWarp = G::kChunksPerWarp;
+    constexpr int kRowsPerWarp = G::kRowsPerWarp;
+    constexpr int kKGroupThreads = kColWarps * 32;
+
     extern __shared__ uint8_t smem_raw[];
     // round up to 1024 bytes by offsetting the shared array itself, so that
     // the compiler still knows every derived pointer is a shared address
     uint8_t *smem = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
-    float *red = reinterpret_cast<float *>(smem + kRedOff);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kBarOff);
-    uint64_t *empty = full + kStages;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStages);
+    const int S = p.stages;
+    const uint32_t SB = p.stage_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (uint32_t)S * SB);
+    uint64_t *empty = full + kMaxStages;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kMaxStages);
     volatile int *duty_ok = abort_flag + 1;
-    volatile uint32_t *consts = reinterpret_cast<volatile uint32_t *>(abort_flag + 2);
+    volatile int *go = abort_flag + 2;
+    volatile uint32_t *consts = reinterpret_cast<volatile uint32_t *>(abort_flag + 3);
 
-    using L = Layout<KG>;
-    constexpr int kConsumerWarps = L::kConsumerWarps;
-    constexpr int kConsumerThreads = L::kConsumerThreads;
-    constexpr int kChunksPerWarp = L::kChunksPerWarp;
-    constexpr int kRowsPerWarp = L::kRowsPerWarp;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int c = blockIdx.x;
@@ -183,12 +192,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     ptx::launch_dependents();
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             ptx::mbar_init(ptx::smem_addr(full + s), 1);
             ptx::mbar_init(ptx::smem_addr(empty + s), kConsumerWarps);
         }
         *abort_flag = 0;
         *duty_ok = 0;
+        *go = 0;
         consts[0] = 0x64006400u;   // 1024.0 in both halves
         consts[1] = 0x54005400u;   // 64.0 in both halves
         ptx::fence_mbar_init();
@@ -204,50 +214,61 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             ptx::prefetch_tmap(&tm_z);
             int tile = first_tile;
             int kb = begin - tile * p.kiters;
-            // The weights, scales and zero points of the first stages do not
-            // depend on the kernel before this one: load them while it
-            // finishes, and the activations once it has.
-            const int pre = n_iters < kStages ? n_iters : kStages;
-            for (int i = 0; i < pre; ++i) {
-                const uint32_t fb = ptx::smem_addr(full + i);
-                const uint32_t st = ptx::smem_addr(smem + i * kStageBytes);
+            int slot = 0, round = 0;
+            auto issue_weights = [&]() {
+                const uint32_t fb = ptx::smem_addr(full + slot);
+                const uint32_t st = ptx::smem_addr(smem + (uint32_t)slot * SB);
                 const int k0 = kb * kStageRows;
                 const int grp0 = k0 / p.g;
                 ptx::mbar_arrive_expect_tx(fb, p.stage_tx);
-                ptx::tma_load_2d(st, &tm_w, fb, tile * kTileWords, k0);
-                ptx::tma_load_2d(st + kSOff, &tm_s, fb, tile * kTileCols, grp0);
-                ptx::tma_load_2d(st + kZOff, &tm_z, fb, tile * kTileWords, grp0);
+                if (CW == 1) {
+                    ptx::tma_load_2d(st, &tm_w, fb, tile * kTileWords, k0);
+                    ptx::tma_load_2d(st + p.s_off, &tm_s, fb, tile * kTileCols, grp0);
+                    ptx::tma_load_2d(st + p.z_off, &tm_z, fb, tile * kTileWords, grp0);
+                } else {
+                    ptx::tma_load_3d(st, &tm_w, fb, 0, tile * CW, k0);
+                    ptx::tma_load_3d(st + p.s_off, &tm_s, fb, 0, tile * CW, grp0);
+                    ptx::tma_load_3d(st + p.z_off, &tm_z, fb, 0, tile * CW, grp0);
+                }
+            };
+            auto issue_x = [&](int sl, int kbx) {
+                ptx::tma_load_3d(ptx::smem_addr(smem + (uint32_t)sl * SB + p.x_off), &tm_x,
+                                 ptx::smem_addr(full + sl), 0, kbx * kKBlocks, 0);
+            };
+            auto advance = [&]() {
                 if (++kb == p.kiters) { kb = 0; ++tile; }
+                if (++slot == S) { slot = 0; ++round; }
+            };
+            // The weights, scales and zero points of the first S stages do
+            // not depend on the kernel before this one: load them while it
+            // finishes, and the activations once it has.
+            const int pre = n_iters < S ? n_iters : S;
+            const int kb_first = kb;
+            for (int i = 0; i < pre; ++i) {
+                issue_weights();
+                advance();
             }
             ptx::wait_prerequisites();
-            for (int i = 0, kx = begin % p.kiters; i < pre; ++i) {
-                ptx::tma_load_3d(ptx::smem_addr(smem + i * kStageBytes + kXOff), &tm_x,
-                                 ptx::smem_addr(full + i), 0, kx * (kStageRows / 64), 0);
+            for (int i = 0, kx = kb_first; i < pre; ++i) {
+                issue_x(i, kx);
                 if (++kx == p.kiters) kx = 0;
             }
             int issued = pre;
             for (int i = pre; i < n_iters; ++i) {
-                const int s = i % kStages;
-                const uint32_t parity = ((i / kStages) & 1) ^ 1;
-                if (!ptx::mbar_wait_bounded(ptx::smem_addr(empty + s), parity, abort_flag, p.status))
+                if (!ptx::mbar_wait_bounded(ptx::smem_addr(empty + slot), (uint32_t)((round - 1) & 1),
+                                            abort_flag, p.status))
                     break;
-                const uint32_t fb = ptx::smem_addr(full + s);
-                const uint32_t st = ptx::smem_addr(smem + s * kStageBytes);
-                const int k0 = kb * kStageRows;
-                const int grp0 = k0 / p.g;
-                ptx::mbar_arrive_expect_tx(fb, p.stage_tx);
-                ptx::tma_load_2d(st, &tm_w, fb, tile * kTileWords, k0);
-                ptx::tma_load_3d(st + kXOff, &tm_x, fb, 0, k0 / 64, 0);
-                ptx::tma_load_2d(st + kSOff, &tm_s, fb, tile * kTileCols, grp0);
-                ptx::tma_load_2d(st + kZOff, &tm_z, fb, tile * kTileWords, grp0);
+                issue_weights();
+                issue_x(slot, kb);
+                advance();
                 issued = i + 1;
-                if (++kb == p.kiters) { kb = 0; ++tile; }
             }
             if (*abort_flag) {
-                // let the copies already in flight land before the CTA exits
-                for (int i = std::max(0, issued - kStages); i < issued; ++i)
-                    ptx::mbar_wait_bounded(ptx::smem_addr(full + i % kStages), (i / kStages) & 1,
-                                           nullptr, nullptr);
+                // let the copies already in flight land before the CTA's
+                // shared memory is released
+                for (int i = std::max(0, issued - S); i < issued; ++i)
+                    ptx::mbar_wait_bounded(ptx::smem_addr(full + i % S), (uint32_t)((i / S) & 1), nullptr,
+                                           nullptr);
             }
         }
         return;
@@ -257,30 +278,37 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     // everything below reads or writes global memory the kernel before this
     // one may still use (activations come through the producer, which waited)
     ptx::wait_prerequisites();
-    const int kg = warp / kColWarps;   // rows kRowsPerWarp * kg .. of every stage
-    const int cw = warp % kColWarps;   // which 64-column quarter of the tile
+    const int kg = warp / kColWarps;   // rows 128 kg .. 128 kg + 127 of every stage
+    const int cw = warp % kColWarps;   // which 64 columns of the tile
     const int gq = lane >> 2;          // MMA groupID: output column pair / token
     const int tq = lane & 3;           // MMA thread-in-group: k pair / token pair
-    const int word = cw * 8 + gq;      // packed word (8 columns) this thread owns
+    const int word = cw * 8 + gq;      // packed word (8 columns) of the tile this thread owns
     const int ct = cw * 32 + lane;     // thread index within a k-group
 
-    // Byte offsets inside a stage. Chunk j of this warp is stage rows
-    // R0 + 16 j .. +15 (R0 = kRowsPerWarp kg); rows 16ch + 2tq (+1) sit at a
-    // fixed 128-byte swizzle phase, rows +8 / +9 one 1024-byte atom further.
+    // Byte offsets of this thread's packed words inside a slot. The weight
+    // area is [row][CW chunks][128 bytes]; 128-byte segment q = row * CW +
+    // chunk holds its 16-byte unit u at unit u ^ (q % 8). Chunk j of this
+    // warp is rows R0 + 16 j .. +15 (R0 = 128 kg); the thread reads rows
+    // 2tq, 2tq + 1 and the same + 8 (one 8-row step keeps q % 8).
     const int R0 = kRowsPerWarp * kg;
-    const uint32_t wchunk = (uint32_t)(word >> 2);
-    const uint32_t inw = (uint32_t)(word & 3) * 4;
-    const uint32_t rA = (uint32_t)(2 * tq), rB = rA + 1;
-    const uint32_t offA = (uint32_t)R0 * 128 + rA * 128 + ((wchunk ^ rA) << 4) + inw;
-    const uint32_t offB = (uint32_t)R0 * 128 + rB * 128 + ((wchunk ^ rB) << 4) + inw;
+    const uint32_t chunk = (uint32_t)(word >> 5);
+    const uint32_t wic = (uint32_t)(word & 31);
+    const uint32_t unit = wic >> 2;
+    const uint32_t inw = (wic & 3) * 4;
+    const uint32_t qA = (uint32_t)(2 * tq) * CW + chunk, qB = (uint32_t)(2 * tq + 1) * CW + chunk;
+    const uint32_t rowbase = (uint32_t)R0 * (CW * 128);
+    const uint32_t offA = rowbase + qA * 128 + ((unit ^ (qA & 7)) << 4) + inw;
+    const uint32_t offB = rowbase + qB * 128 + ((unit ^ (qB & 7)) << 4) + inw;
+    constexpr uint32_t kChunkStride = 16 * CW * 128;   // 16 rows
+    constexpr uint32_t kRow8 = 8 * CW * 128;           // 8 rows
     // activation slice: [token m][64-row block][64 halves], 128-byte rows
-    // (r = m * 4 + block), 16-byte unit u of row r stored at unit u ^ (r % 8).
-    // Chunk j of this warp is block R0 / 64 + j / 4, units 2 (j % 4) and
-    // 2 (j % 4) + 1 -- the k 0..7 and 8..15 halves of its B operand. One
-    // ldmatrix.x4 fetches the B operands of a chunk pair for eight tokens:
-    // lane L addresses token L % 8, unit 4 * pair + L / 8 of the block.
-    constexpr int kBlocksPerWarp = (kChunksPerWarp + 3) / 4;
-    static_assert(kChunksPerWarp % 2 == 0, "chunks are fetched in pairs");
+    // (r = m * kKBlocks + block), 16-byte unit u of row r stored at unit
+    // u ^ (r % 8). Chunk j of this warp is block R0 / 64 + j / 4, units
+    // 2 (j % 4) and 2 (j % 4) + 1 -- the k 0..7 and 8..15 halves of its B
+    // operand. One ldmatrix.x4 fetches the B operands of a chunk pair for
+    // eight tokens: lane L addresses token L % 8, unit 4 * pair + L / 8.
+    constexpr int kBlocksPerWarp = kChunksPerWarp / 4;
+    static_assert(kChunksPerWarp % 4 == 0, "whole 64-row activation blocks per warp and stage");
     uint32_t xoff[MT][kBlocksPerWarp][2];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
@@ -289,10 +317,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             const uint32_t r = (uint32_t)((8 * mt + (lane & 7)) * kKBlocks + R0 / 64 + jb);
 #pragma unroll
             for (int pr = 0; pr < 2; ++pr)
-                xoff[mt][jb][pr] = kXOff + r * 128 + (((uint32_t)(4 * pr + (lane >> 3)) ^ (r & 7)) << 4);
+                xoff[mt][jb][pr] = p.x_off + r * 128 + (((uint32_t)(4 * pr + (lane >> 3)) ^ (r & 7)) << 4);
         }
-    const uint32_t soff = kSOff + (uint32_t)word * 16;
-    const uint32_t zoff = kZOff + (uint32_t)word * 4;
+    const uint32_t soff = p.s_off + (uint32_t)word * 16;
+    const uint32_t zoff = p.z_off + (uint32_t)word * 4;
     // the fp16 exponent patterns OR-ed into the nibbles, read from shared
     // memory so that they stay in registers instead of being rebuilt before
     // every use (a LOP3 takes only one immediate operand)
@@ -308,6 +336,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     int seg_kb0 = 0;
     int tile = first_tile;
     int kb = begin - tile * p.kiters;
+    int slot = 0;
+    uint32_t phase = 0;
 
     // loads this thread's 8 scales and zero points of group row r of a stage
     auto load_group = [&](const uint8_t *stp, uint32_t r) {
@@ -348,16 +378,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             wg_rem += kStageRows;
             while (wg_rem >= p.g) { wg_rem -= p.g; ++wg_grp; }
         }
-        const int s = i % kStages;
+        uint8_t *stp = smem + (uint32_t)slot * SB;
         // every lane waits (each needs the acquire); the MMA below is
         // warp-wide, so the outcome is made uniform across the warp
         const bool ok = __all_sync(0xffffffffu,
-                                   ptx::mbar_wait_bounded(ptx::smem_addr(full + s), (i / kStages) & 1,
+                                   ptx::mbar_wait_bounded(ptx::smem_addr(full + slot), phase,
                                                           abort_flag, p.status));
         if (ok && k0 + R0 < p.K) {
-            const uint8_t *stp = smem + s * kStageBytes;
             if (kWholeGroups) {
-                // g % kRowsPerWarp == 0: the warp's rows lie in one group
+                // g % 128 == 0: the warp's rows lie in one group
                 if (wg_grp != loaded_grp) {
                     loaded_grp = wg_grp;
                     load_group(stp, (uint32_t)(wg_grp - st_grp));
@@ -378,11 +407,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                         load_group(stp, (uint32_t)(grp - st_grp));
                     }
                 }
-                const uint8_t *wp = stp + j * (16 * 128);
+                const uint8_t *wp = stp + j * kChunkStride;
                 const uint32_t v0 = *reinterpret_cast<const uint32_t *>(wp + offA);
                 const uint32_t v1 = *reinterpret_cast<const uint32_t *>(wp + offB);
-                const uint32_t v8 = *reinterpret_cast<const uint32_t *>(wp + offA + 1024);
-                const uint32_t v9 = *reinterpret_cast<const uint32_t *>(wp + offB + 1024);
+                const uint32_t v8 = *reinterpret_cast<const uint32_t *>(wp + offA + kRow8);
+                const uint32_t v9 = *reinterpret_cast<const uint32_t *>(wp + offB + kRow8);
                 if ((j & 1) == 0) {
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt)
@@ -409,25 +438,29 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(empty + s));
+        const bool seg_end = (i == n_iters - 1 || kb == p.kiters - 1);
+        if (!seg_end || KG == 1) {
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(empty + slot));
+        }
 
-        if (i == n_iters - 1 || kb == p.kiters - 1) {
-            // ---- segment end: fold the k-groups into group 0, in the fixed
-            //      order (g0 + g2) + (g1 + g3) for four groups
-            if (KG == 4) {
-                if (kg >= 2) fold_store<MT>(red + (kg - 2) * kFoldFloats, acc, ct);
+        if (seg_end) {
+            if (KG == 2) {
+                // ---- fold k-group 1 into k-group 0 through this slot's weight
+                //      area (every warp has finished reading it at the first
+                //      barrier), then release the slot
+                float *red = reinterpret_cast<float *>(stp);
                 ptx::named_barrier(1, kConsumerThreads);
-                if (kg < 2) fold_add<MT>(red + kg * kFoldFloats, acc, ct);
+                if (kg == 1) fold_store<MT, kKGroupThreads>(red, acc, ct);
                 ptx::named_barrier(1, kConsumerThreads);
+                if (kg == 0) fold_add<MT, kKGroupThreads>(red, acc, ct);
+                // generic-proxy accesses to the slot are ordered before the
+                // TMA writes that refill it
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(empty + slot));
             }
-            if (kg == 1) fold_store<MT>(red, acc, ct);
-            ptx::named_barrier(1, kConsumerThreads);
-            if (kg == 0) fold_add<MT>(red, acc, ct);
-            ptx::named_barrier(1, kConsumerThreads);
 
-            // `whole` is uniform across the CTA; barrier participation never
-            // depends on the abort flag, which other warps may set at any time
             const bool whole = (seg_kb0 == 0 && kb == p.kiters - 1);
             if (kg == 0) {
                 const bool live = !*abort_flag;
@@ -460,7 +493,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                         }
                 } else if (!whole && live) {
                     const int which = (tile == first_tile) ? 0 : 1;
-                    float *slot = p.partials + (int64_t)(2 * c + which) * kPartialFloats;
+                    float *pslot = p.partials + (int64_t)(2 * c + which) * G::kPartialFloats;
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -469,7 +502,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                             if (m < p.M) {
                                 float4 lo = make_float4(acc[0][mt][e], acc[0][mt][2 + e], acc[1][mt][e], acc[1][mt][2 + e]);
                                 float4 hi = make_float4(acc[2][mt][e], acc[2][mt][2 + e], acc[3][mt][e], acc[3][mt][2 + e]);
-                                float4 *dst = reinterpret_cast<float4 *>(slot + m * kTileCols + word * 8);
+                                float4 *dst = reinterpret_cast<float4 *>(pslot + m * kTileCols + word * 8);
                                 dst[0] = lo;
                                 dst[1] = hi;
                             }
@@ -477,7 +510,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                     __threadfence();
                 }
                 if (!whole) {
-                    ptx::named_barrier(2, kConsumerThreads / KG);
+                    ptx::named_barrier(2, kKGroupThreads);
                     // count in with the tile's finisher (not needed for its own tile)
                     if (ct == 0 && !*abort_flag && !(reducer && tile == first_tile))
                         atomicAdd(p.arrive + tile, 1u);
@@ -485,28 +518,35 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             }
         }
         if (++kb == p.kiters) { kb = 0; ++tile; }
+        if (++slot == S) { slot = 0; phase ^= 1u; }
     }
+
+    // One consumer thread decides, for all of them, whether the CTA goes on
+    // (the producer may still set the abort flag while the others read it).
+    const int ctid = threadIdx.x;   // 0 .. kConsumerThreads - 1
+    ptx::named_barrier(1, kConsumerThreads);
+    if (ctid == 0) *go = *abort_flag ? 0 : 1;
+    ptx::named_barrier(1, kConsumerThreads);
+    if (!*go) return;
 
     // ---- finishing the split tile this range starts in: wait for the other
     //      contributors (lower-numbered CTAs) to count in, then sum every
     //      partial, its own included, in contributor order, so the result
     //      does not depend on timing; add the bias and round once.
     if (!reducer) return;
-    const int ctid = threadIdx.x;   // 0 .. kConsumerThreads-1
     const int t = first_tile;
     const int cf = cta_of(t * p.kiters, p.total, p.ctas);
     const int n = c - cf + 1;
     if (ctid == 0) {
-        bool ok = !*abort_flag;
+        bool ok = true;
         const long long t0 = clock64();
-        while (ok && ptx::ld_acquire_gpu(p.arrive + t) < (unsigned)(n - 1)) {
-            if (*abort_flag || clock64() - t0 > ptx::kWaitLimitCycles) {
+        while (ptx::ld_acquire_gpu(p.arrive + t) < (unsigned)(n - 1)) {
+            if (clock64() - t0 > ptx::kWaitLimitCycles) {
                 ok = false;
-                *abort_flag = 1;
                 atomicOr(p.status, kStatusTimeout);
-            } else {
-                __nanosleep(32);
+                break;
             }
+            __nanosleep(32);
         }
         *duty_ok = ok ? 1 : 0;
     }
@@ -522,7 +562,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     const int which_cf = (range_begin(cf, p.total, p.ctas) / p.kiters == t) ? 0 : 1;
     constexpr int kPosPerThread = (kMaxTokens * kTileCols / 4 + kConsumerThreads - 1) / kConsumerThreads;
     const int n4 = p.M * (kTileCols / 4);   // float4 positions of one partial
-    const int per_round = (kStages * kStageBytes) / (n4 * 16);
+    const int per_round = (int)(((uint32_t)S * SB) / (uint32_t)(n4 * 16));
     const uint32_t ring = ptx::smem_addr(smem);
     float4 acc4[kPosPerThread];
 #pragma unroll
@@ -531,13 +571,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         const int cnt = std::min(per_round, n - r0);
         for (int q = 0; q < cnt; ++q) {
             const int ci = cf + r0 + q;
-            const float *slot = p.partials + (int64_t)(2 * ci + (ci == cf ? which_cf : 0)) * kPartialFloats;
+            const float *src = p.partials + (int64_t)(2 * ci + (ci == cf ? which_cf : 0)) * G::kPartialFloats;
 #pragma unroll
             for (int k = 0; k < kPosPerThread; ++k) {
                 const int pos = ctid + k * kConsumerThreads;
                 if (pos < n4)
                     ptx::cp_async_16(ring + (uint32_t)(q * n4 + pos) * 16,
-                                     slot + (pos / (kTileCols / 4)) * kTileCols + (pos % (kTileCols / 4)) * 4);
+                                     src + (pos / (kTileCols / 4)) * kTileCols + (pos % (kTileCols / 4)) * 4);
             }
         }
         ptx::cp_async_wait_all();
@@ -558,7 +598,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         if (pos >= n4) continue;
         const int m = pos / (kTileCols / 4);
         const int col = t * kTileCols + (pos % (kTileCols / 4)) * 4;
-        if (col >= p.N || *abort_flag) continue;
+        if (col >= p.N) continue;
         float b[4] = {0.f, 0.f, 0.f, 0.f};
         if (p.bias) {
             const uint2 braw = *reinterpret_cast<const uint2 *>(p.bias + col);
@@ -613,45 +653,72 @@ bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, int rank
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Largest number of groups one stage can touch.
-int group_rows_per_stage(int64_t g)
+// Largest number of groups a stage of `rows` k-rows can touch.
+int group_rows_per_stage(int64_t g, int rows)
 {
-    if (kStageRows % g == 0) return (int)(kStageRows / g);
-    if (g % kStageRows == 0) return 1;
-    return (int)((kStageRows - 1) / g + 2);
+    if (rows % g == 0) return (int)(rows / g);
+    if (g % rows == 0) return 1;
+    return (int)((rows - 1) / g + 2);
 }
 
-// The four tensor maps of a launch and the bytes one stage delivers.
+// The tensor maps of a launch and the slot layout. CW = 1 uses 2-D maps
+// (any N % 32 == 0; the last tile reads past N as zeros); CW = 2 views the
+// row-major arrays as [rows][N / 256][256 columns] (N % 512 == 0).
+template <int CW>
 bool build_maps(const Problem &pr, int mpad, CUtensorMap *tw, CUtensorMap *tx, CUtensorMap *ts,
-                CUtensorMap *tz, uint32_t *stage_tx)
+                CUtensorMap *tz, DecodeParams *p)
 {
-    const uint64_t K = (uint64_t)pr.K, N = (uint64_t)pr.N, M = (uint64_t)pr.M, G = (uint64_t)pr.G;
-    const int R = group_rows_per_stage(pr.g);
-    const uint64_t wd[2] = {N / 8, K}, ws[1] = {N / 2};
-    const uint32_t wb[2] = {kTileWords, kStageRows};
-    // x viewed as [M][K / 64][64]: one box covers a stage's 256 k for every token
+    using G = Geo<CW>;
+    const uint64_t K = (uint64_t)pr.K, N = (uint64_t)pr.N, M = (uint64_t)pr.M, Gn = (uint64_t)pr.G;
+    const int R = group_rows_per_stage(pr.g, G::kStageRows);
+    // x viewed as [M][K / 64][64]: one box covers a stage's k for every token
     const uint64_t xd[3] = {64, K / 64, M}, xs[2] = {128, K * 2};
-    const uint32_t xb[3] = {64, kKBlocks, (uint32_t)mpad};
-    const uint64_t sd[2] = {N, G}, ss[1] = {N * 2};
-    const uint32_t sb[2] = {kTileCols, (uint32_t)R};
-    const uint64_t zd[2] = {N / 8, G}, zs[1] = {N / 2};
-    const uint32_t zb[2] = {kTileWords, (uint32_t)R};
-    *stage_tx = (uint32_t)(kWBytes + mpad * kStageRows * 2 + R * (kTileCols * 2) + R * (kTileWords * 4));
-    return make_map(tw, CU_TENSOR_MAP_DATA_TYPE_INT32, pr.qweight, 2, wd, ws, wb, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_map(tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.x, 3, xd, xs, xb, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_map(ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.scales, 2, sd, ss, sb, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-           make_map(tz, CU_TENSOR_MAP_DATA_TYPE_INT32, pr.qzeros, 2, zd, zs, zb, CU_TENSOR_MAP_SWIZZLE_NONE);
+    const uint32_t xb[3] = {64, (uint32_t)G::kKBlocks, (uint32_t)mpad};
+    bool ok = make_map(tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.x, 3, xd, xs, xb, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (CW == 1) {
+        const uint64_t wd[2] = {N / 8, K}, ws[1] = {N / 2};
+        const uint32_t wb[2] = {(uint32_t)G::kTileWords, (uint32_t)G::kStageRows};
+        const uint64_t sd[2] = {N, Gn}, ss[1] = {N * 2};
+        const uint32_t sb[2] = {(uint32_t)G::kTileCols, (uint32_t)R};
+        const uint64_t zd[2] = {N / 8, Gn}, zs[1] = {N / 2};
+        const uint32_t zb[2] = {(uint32_t)G::kTileWords, (uint32_t)R};
+        ok = ok && make_map(tw, CU_TENSOR_MAP_DATA_TYPE_INT32, pr.qweight, 2, wd, ws, wb, CU_TENSOR_MAP_SWIZZLE_128B) &&
+             make_map(ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.scales, 2, sd, ss, sb, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+             make_map(tz, CU_TENSOR_MAP_DATA_TYPE_INT32, pr.qzeros, 2, zd, zs, zb, CU_TENSOR_MAP_SWIZZLE_NONE);
+    } else {
+        const uint64_t wd[3] = {32, N / 256, K}, ws[2] = {128, N / 2};
+        const uint32_t wb[3] = {32, (uint32_t)CW, (uint32_t)G::kStageRows};
+        const uint64_t sd[3] = {256, N / 256, Gn}, ss[2] = {512, N * 2};
+        const uint32_t sb[3] = {256, (uint32_t)CW, (uint32_t)R};
+        const uint64_t zd[3] = {32, N / 256, Gn}, zs[2] = {128, N / 2};
+        const uint32_t zb[3] = {32, (uint32_t)CW, (uint32_t)R};
+        ok = ok && make_map(tw, CU_TENSOR_MAP_DATA_TYPE_INT32, pr.qweight, 3, wd, ws, wb, CU_TENSOR_MAP_SWIZZLE_128B) &&
+             make_map(ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.scales, 3, sd, ss, sb, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+             make_map(tz, CU_TENSOR_MAP_DATA_TYPE_INT32, pr.qzeros, 3, zd, zs, zb, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    // slot: weights | activations | scale rows | zero rows, 1024-aligned
+    const uint32_t xbytes = (uint32_t)(mpad * G::kStageRows * 2);
+    const uint32_t sbytes = (uint32_t)(R * G::kTileCols * 2);
+    const uint32_t zbytes = (uint32_t)(R * G::kTileWords * 4);
+    p->x_off = kWBytes;
+    p->s_off = p->x_off + xbytes;
+    p->z_off = p->s_off + sbytes;
+    p->stage_bytes = (p->z_off + zbytes + 1023u) & ~1023u;
+    p->stages = std::min<int>(kMaxStages, (kSmemLimit - kBarBytes - 1024) / (int)p->stage_bytes);
+    p->stage_tx = kWBytes + xbytes + sbytes + zbytes;
+    return ok && p->stages >= 2;
 }
+
+uint32_t smem_bytes(const DecodeParams &p) { return (uint32_t)p.stages * p.stage_bytes + kBarBytes + 1024; }
 
 // Per (device, kernel variant): dynamic shared memory opted in once, and the
-// number of resident CTAs per SM with the SM count.
+// SM count.
 struct LaunchInfo {
-    int occ = 0;
     int sms = 0;
     cudaError_t err = cudaSuccess;
 };
 
-template <int MT, int KG, bool WG>
+template <int MT, int CW, bool WG>
 LaunchInfo launch_info()
 {
     static std::mutex mu;
@@ -663,47 +730,48 @@ LaunchInfo launch_info()
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(dev);
     if (it != cache.end()) return it->second;
-    auto kern = decode_kernel<MT, KG, WG>;
-    li.err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    auto kern = decode_kernel<MT, CW, WG>;
+    li.err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (li.err == cudaSuccess)
         li.err = cudaDeviceGetAttribute(&li.sms, cudaDevAttrMultiProcessorCount, dev);
+    int occ = 0;
     if (li.err == cudaSuccess)
-        li.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&li.occ, kern, Layout<KG>::kThreads, kSmemBytes);
-    if (li.err == cudaSuccess && li.occ < 1) li.err = cudaErrorLaunchOutOfResources;
+        li.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, kSmemLimit);
+    if (li.err == cudaSuccess && occ < 1) li.err = cudaErrorLaunchOutOfResources;
     if (li.err == cudaSuccess) cache[dev] = li;
     return li;
 }
 
-// Fills everything but the scratch pointers; the grid size goes to p->ctas.
-template <int MT, int KG, bool WG>
+// Fills everything but the scratch pointers; the grid size goes to p->ctas
+// (one CTA per SM).
+template <int MT, int CW, bool WG>
 cudaError_t prepare(const Problem &pr, int max_ctas, CUtensorMap *maps, DecodeParams *p)
 {
-    const LaunchInfo li = launch_info<MT, KG, WG>();
+    using G = Geo<CW>;
+    const LaunchInfo li = launch_info<MT, CW, WG>();
     if (li.err != cudaSuccess) return li.err;
-    const int tiles = (int)((pr.N + kTileCols - 1) / kTileCols);
-    const int kiters = (int)((pr.K + kStageRows - 1) / kStageRows);
+    const int tiles = (int)((pr.N + G::kTileCols - 1) / G::kTileCols);
+    const int kiters = (int)((pr.K + G::kStageRows - 1) / G::kStageRows);
     const int64_t total = (int64_t)tiles * kiters;
-    const int ctas = (int)std::min<int64_t>(std::min<int64_t>(total, (int64_t)li.occ * li.sms), max_ctas);
-    uint32_t stage_tx = 0;
-    if (!build_maps(pr, 8 * MT, &maps[0], &maps[1], &maps[2], &maps[3], &stage_tx))
-        return cudaErrorInvalidValue;
+    const int ctas = (int)std::min<int64_t>(std::min<int64_t>(total, (int64_t)li.sms), max_ctas);
     *p = DecodeParams{};
+    if (!build_maps<CW>(pr, 8 * MT, &maps[0], &maps[1], &maps[2], &maps[3], p))
+        return cudaErrorInvalidValue;
     p->bias = static_cast<const __half *>(pr.bias);
     p->y = static_cast<__half *>(pr.y);
     p->status = device_status_word();
     p->M = (int)pr.M; p->K = (int)pr.K; p->N = (int)pr.N; p->g = (int)pr.g;
     p->tiles = tiles; p->kiters = kiters; p->total = (int)total; p->ctas = ctas;
-    p->stage_tx = stage_tx;
     return cudaSuccess;
 }
 
-template <int MT, int KG, bool WG>
+template <int MT, int CW, bool WG>
 cudaError_t launch_kernel(const CUtensorMap *maps, const DecodeParams &p, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)p.ctas);
-    cfg.blockDim = dim3(Layout<KG>::kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes(p);
     cfg.stream = stream;
     // programmatic dependent launch: the kernel starts streaming weights while
     // the previous kernel on the stream drains (it waits for it before
@@ -713,38 +781,42 @@ cudaError_t launch_kernel(const CUtensorMap *maps, const DecodeParams &p, cudaSt
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<MT, KG, WG>, maps[0], maps[1], maps[2], maps[3], p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<MT, CW, WG>, maps[0], maps[1], maps[2], maps[3], p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-template <int MT, int KG, bool WG>
+template <int MT, int CW, bool WG>
 cudaError_t launch_decode_t(const Problem &pr, cudaStream_t stream)
 {
     CUtensorMap maps[4];
     DecodeParams p;
-    cudaError_t e = prepare<MT, KG, WG>(pr, 1 << 30, maps, &p);
+    cudaError_t e = prepare<MT, CW, WG>(pr, 1 << 30, maps, &p);
     if (e != cudaSuccess) return e;
     Scratch sc{};
-    if (!get_scratch(stream, (size_t)2 * p.ctas * kPartialFloats, (size_t)p.tiles, &sc))
+    // sized for the widest tile, so that the area never grows between the
+    // first call on a stream and a later graph capture of other shapes
+    if (!get_scratch(stream, (size_t)2 * p.ctas * kMaxPartialFloats, (size_t)p.tiles, &sc))
         return cudaErrorMemoryAllocation;
     p.partials = sc.partials;
     p.arrive = sc.counters;
-    return launch_kernel<MT, KG, WG>(maps, p, stream);
+    return launch_kernel<MT, CW, WG>(maps, p, stream);
 }
 
-// Consumer k-groups. Two (8 consumer warps + the producer, up to 168
-// registers a thread) ran a little faster than four (16 + 1 warps, held to
-// 96 registers, which spilled at two token tiles) for every decode shape.
-template <int MT> struct KGroupsFor { static constexpr int value = 2; };
+// Tile width: 512 columns for very wide matrices (rows 256 bytes wide read
+// HBM closer to its copy bandwidth: 3-5 % faster at N = 57344), 256 otherwise
+// (fewer CTAs share a tile, so split-K finishing stays short; 512-column
+// tiles measured 2-10 % slower at N = 10240..22016).
+bool wide_tiles(int64_t N) { return N % 512 == 0 && N >= 32768; }
 
-// whole: g divides the rows each warp takes per stage into one group
+// whole: every warp's 128 rows of a stage lie in one group
 template <int MT>
 cudaError_t dispatch_decode(const Problem &p, cudaStream_t stream)
 {
-    constexpr int KG = KGroupsFor<MT>::value;
-    const bool whole = p.g % Layout<KG>::kRowsPerWarp == 0;
-    return whole ? launch_decode_t<MT, KG, true>(p, stream) : launch_decode_t<MT, KG, false>(p, stream);
+    const bool whole = p.g % 128 == 0;
+    if (wide_tiles(p.N))
+        return whole ? launch_decode_t<MT, 2, true>(p, stream) : launch_decode_t<MT, 2, false>(p, stream);
+    return whole ? launch_decode_t<MT, 1, true>(p, stream) : launch_decode_t<MT, 1, false>(p, stream);
 }
 
 } // namespace
@@ -752,9 +824,10 @@ cudaError_t dispatch_decode(const Problem &p, cudaStream_t stream)
 bool decode_supported(int64_t M, int64_t K, int64_t N, int64_t g)
 {
     return M >= 1 && M <= kMaxTokens && K % 64 == 0 && N % 32 == 0 && g % 16 == 0 &&
-           group_rows_per_stage(g) <= kMaxGroupRows && K <= (int64_t(1) << 30) &&
+           group_rows_per_stage(g, Geo<1>::kStageRows) <= kMaxGroupRows && K <= (int64_t(1) << 30) &&
            N <= (int64_t(1) << 30) &&
-           ((K + kStageRows - 1) / kStageRows) * ((N + kTileCols - 1) / kTileCols) < (int64_t(1) << 31);
+           ((K + Geo<1>::kStageRows - 1) / Geo<1>::kStageRows) * ((N + Geo<1>::kTileCols - 1) / Geo<1>::kTileCols) <
+               (int64_t(1) << 30);
 }
 
 cudaError_t launch_decode(const Problem &p, cudaStream_t stream)
@@ -778,7 +851,7 @@ namespace {
 
 constexpr int kNoAllocMaxCtas = 160;    // grid cap: partial slots for 160 CTAs
 constexpr int kNoAllocMaxTiles = 8192;  // 256-column tiles: N up to 2,097,152
-constexpr size_t kNoAllocPartialWords = (size_t)2 * kNoAllocMaxCtas * kPartialFloats;
+constexpr size_t kNoAllocPartialWords = (size_t)2 * kNoAllocMaxCtas * Geo<1>::kPartialFloats;
 constexpr size_t kNoAllocWords = kNoAllocPartialWords + (size_t)kNoAllocMaxTiles;
 
 // fp32 partials (2 slots per CTA) followed by the arrival counter of every
@@ -810,12 +883,12 @@ cudaError_t noalloc_scratch_address(uint32_t **out)
     return cudaSuccess;
 }
 
-template <int MT, int KG, bool WG>
+template <int MT, bool WG>
 cudaError_t launch_decode_noalloc_t(const Problem &pr, cudaStream_t stream, uint32_t *scratch)
 {
     CUtensorMap maps[4];
     DecodeParams p;
-    cudaError_t e = prepare<MT, KG, WG>(pr, kNoAllocMaxCtas, maps, &p);
+    cudaError_t e = prepare<MT, 1, WG>(pr, kNoAllocMaxCtas, maps, &p);
     if (e != cudaSuccess) return e;
     p.partials = reinterpret_cast<float *>(scratch);
     p.arrive = scratch + kNoAllocPartialWords;
@@ -823,16 +896,16 @@ cudaError_t launch_decode_noalloc_t(const Problem &pr, cudaStream_t stream, uint
     // start at zero (the partial slots are always written before being read)
     e = cudaMemsetAsync(p.arrive, 0, sizeof(uint32_t) * (size_t)p.tiles, stream);
     if (e != cudaSuccess) return e;
-    return launch_kernel<MT, KG, WG>(maps, p, stream);
+    return launch_kernel<MT, 1, WG>(maps, p, stream);
 }
 
 template <int MT>
 cudaError_t dispatch_noalloc(const Problem &p, cudaStream_t stream, uint32_t *scratch)
 {
-    constexpr int KG = KGroupsFor<MT>::value;
-    const bool whole = p.g % Layout<KG>::kRowsPerWarp == 0;
-    return whole ? launch_decode_noalloc_t<MT, KG, true>(p, stream, scratch)
-                 : launch_decode_noalloc_t<MT, KG, false>(p, stream, scratch);
+    // always 256-column tiles: the fixed array holds partials of that width
+    const bool whole = p.g % 128 == 0;
+    return whole ? launch_decode_noalloc_t<MT, true>(p, stream, scratch)
+                 : launch_decode_noalloc_t<MT, false>(p, stream, scratch);
 }
 
 bool aligned16_ptr(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -855,7 +928,7 @@ extern "C" awq_status_t awq_linear_forward_decode_noalloc(
         !awq::aligned16_ptr(scales) || !awq::aligned16_ptr(y) || (bias && !awq::aligned16_ptr(bias)))
         return AWQ_ERR_MISALIGNED;
     if (!awq::decode_supported(M, K, N, g)) return AWQ_ERR_INVALID_ARG;
-    if ((N + awq::kTileCols - 1) / awq::kTileCols > awq::kNoAllocMaxTiles) return AWQ_ERR_TOO_LARGE;
+    if ((N + awq::Geo<1>::kTileCols - 1) / awq::Geo<1>::kTileCols > awq::kNoAllocMaxTiles) return AWQ_ERR_TOO_LARGE;
     uint32_t *scratch = nullptr;
     if (awq::noalloc_scratch_address(&scratch) != cudaSuccess) return AWQ_ERR_CUDA;
     awq::Problem p{x, qweight, qzeros, scales, bias, y, M, K, N, g, K / g};

@@ -117,9 +117,61 @@ struct PrefillParams {
     const __half *bias;
     __half *y;
     unsigned int *status;
+    float *partials;        // [2 * sk_ctas][kPartialFloats] stream-K partial sums
+    unsigned int *arrive;   // [sk_tiles] contributors counted in (zero between calls)
     int M, K, N, g;
     int tiles_m, tiles_n, kiters;
+    int dp_waves;           // full waves of whole tiles, tile = cta + wave * gridDim.x
+    int sk_tiles;           // tiles after those, split along k between sk_ctas CTAs
+    int sk_ctas;
     uint32_t stage_tx;
+};
+
+// One stream-K partial: 128 rows x 256 accumulator columns, fp32, laid out
+// [32-column chunk][4-column group][row][4] so that the 32 epilogue lanes of
+// a warp (32 consecutive rows) touch 512 consecutive bytes per access.
+constexpr int kPartialFloats = BM * BN;
+
+__device__ __forceinline__ int sk_range_begin(int c, int units, int ctas) {
+    return (int)(((int64_t)c * units) / ctas);
+}
+// The CTA whose stream-K range contains unit u.
+__device__ __forceinline__ int sk_cta_of(int u, int units, int ctas) {
+    return (int)((((int64_t)u + 1) * ctas - 1) / units);
+}
+
+// The work of one CTA as a list of segments (tile, k-stages kb0 .. kb1 - 1):
+// first its whole tiles of the data-parallel waves, then the pieces of its
+// stream-K range, split at tile boundaries. Every warp role walks the same
+// list.
+struct Segments {
+    int dp;            // whole tiles first
+    int ub, ue;        // stream-K units [ub, ue)
+    int count;
+    __device__ Segments(const PrefillParams &p) {
+        dp = p.dp_waves;
+        const int units = p.sk_tiles * p.kiters;
+        if ((int)blockIdx.x < p.sk_ctas) {
+            ub = sk_range_begin(blockIdx.x, units, p.sk_ctas);
+            ue = sk_range_begin(blockIdx.x + 1, units, p.sk_ctas);
+        } else {
+            ub = ue = 0;
+        }
+        count = dp + (ue > ub ? (ue - 1) / p.kiters - ub / p.kiters + 1 : 0);
+    }
+    // segment i: tile index (0 .. tiles - 1) and its k-stage range
+    __device__ void get(const PrefillParams &p, int i, int &tile, int &kb0, int &kb1) const {
+        if (i < dp) {
+            tile = blockIdx.x + i * gridDim.x;
+            kb0 = 0;
+            kb1 = p.kiters;
+            return;
+        }
+        const int t = ub / p.kiters + (i - dp);   // stream-K tile
+        kb0 = (i == dp) ? ub % p.kiters : 0;
+        kb1 = (t == (ue - 1) / p.kiters) ? (ue - 1) % p.kiters + 1 : p.kiters;
+        tile = p.dp_waves * gridDim.x + t;
+    }
 };
 
 __device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
@@ -185,10 +237,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     uint64_t *drain = acc_empty + 2;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *fix_count = abort_flag + 1;        // stream-K tiles this CTA finishes
+    volatile int *fix_tiles = abort_flag + 2;        // [2]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int n_tiles = p.tiles_m * p.tiles_n;
+    const Segments sg(p);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -203,6 +257,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         }
         ptx::mbar_init(ptx::smem_addr(drain), 1);
         *abort_flag = 0;
+        *fix_count = 0;
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -225,10 +280,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             }
             int it = 0, issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+            for (int si = 0; si < sg.count && ok; ++si) {
+                int tile, kb0, kb1;
+                sg.get(p, si, tile, kb0, kb1);
                 const int m0 = (tile % p.tiles_m) * BM;
                 const int n0 = (tile / p.tiles_m) * BN;
-                for (int kb = 0; kb < p.kiters; ++kb, ++it) {
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
                     if (!ptx::mbar_wait_bounded(ptx::smem_addr(tfree + s), ((it / kStages) & 1) ^ 1,
                                                 abort_flag, p.status)) {
@@ -264,7 +321,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         if (lane == 0) {
             int it = 0, acc_it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++acc_it) {
+            for (int si = 0; si < sg.count && ok; ++si, ++acc_it) {
+                int tile, kb0, kb1;
+                sg.get(p, si, tile, kb0, kb1);
                 const int abuf = acc_it & 1;
                 if (!ptx::mbar_wait_bounded(ptx::smem_addr(acc_empty + abuf), ((acc_it >> 1) & 1) ^ 1,
                                             abort_flag, p.status)) {
@@ -273,7 +332,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 }
                 tc::fence_after_sync();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(abuf * BN);
-                for (int kb = 0; kb < p.kiters; ++kb, ++it) {
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
                     const int b = it & 1;
                     bool ready = ptx::mbar_wait_bounded(ptx::smem_addr(full + s), (it / kStages) & 1,
@@ -294,11 +353,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         const uint64_t ad = tc::smem_desc_sw128(st + C::kAOff + kk * 32, 16, 1024);
                         const uint64_t bd = tc::smem_desc_sw128(bt + kk * 2 * kBKGroupStride,
                                                                 kBAtomStride, kBKGroupStride);
-                        tc::mma_f16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                        tc::mma_f16(d_tmem, ad, bd, kIdesc, (kb != kb0 || kk != 0) ? 1u : 0u);
                     }
                     tc::commit(ptx::smem_addr(tfree + s));
                     if (kDequant) tc::commit(ptx::smem_addr(bfree + b));
-                    if (kb == p.kiters - 1) tc::commit(ptx::smem_addr(acc_full + abuf));
+                    if (kb == kb1 - 1) tc::commit(ptx::smem_addr(acc_full + abuf));
                 }
             }
             // every MMA this thread issued has completed once `drain` flips
@@ -320,8 +379,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             const uint32_t z_in = C::kZOff + (uint32_t)j * 4;
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-                for (int kb = 0; kb < p.kiters; ++kb, ++it) {
+            for (int si = 0; si < sg.count && ok; ++si) {
+                int tile, kb0, kb1;
+                sg.get(p, si, tile, kb0, kb1);
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
                     const int b = it & 1;
                     bool ready = ptx::mbar_wait_bounded(ptx::smem_addr(full + s), (it / kStages) & 1,
@@ -374,50 +435,185 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                 // TMEM lane quarter this warp may read
+        const int et = threadIdx.x - kEpilogueWarp0 * 32;   // 0..127
+        const int sk_units = p.sk_tiles * p.kiters;
         int acc_it = 0;
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++acc_it) {
+        for (int si = 0; si < sg.count; ++si, ++acc_it) {
+            int tile, kb0, kb1;
+            sg.get(p, si, tile, kb0, kb1);
             const int abuf = acc_it & 1;
-            const bool ok = __all_sync(0xffffffffu,
-                                       ptx::mbar_wait_bounded(ptx::smem_addr(acc_full + abuf),
-                                                              (acc_it >> 1) & 1, abort_flag, p.status));
+            // the decision to go on is taken together by the four warps, which
+            // meet at named barriers below
+            const bool ok = ptx::named_barrier_and(
+                1, kEpilogueThreads,
+                ptx::mbar_wait_bounded(ptx::smem_addr(acc_full + abuf), (acc_it >> 1) & 1, abort_flag, p.status));
             if (!ok) break;
             tc::fence_after_sync();
             const int m0 = (tile % p.tiles_m) * BM;
             const int n0 = (tile / p.tiles_m) * BN;
             const int m = m0 + 32 * q + lane;
+            const uint32_t t_acc = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(abuf * BN);
+            if (kb0 == 0 && kb1 == p.kiters) {
+                // ---- whole tile: + bias, one rounding, store
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t raw[32];
+                    tc::ld_32x32b_x32(t_acc + (uint32_t)(32 * c), raw);
+                    tc::ld_wait();
+                    uint32_t r[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = kDequant ? raw[(e & ~7) + unperm(e & 7)] : raw[e];
+                    const int col = n0 + 32 * c;
+                    if (col < p.N && m < p.M) {
+                        __align__(16) __half out[32];
+                        if (p.bias) {
+                            __align__(16) __half bh[32];
+#pragma unroll
+                            for (int v = 0; v < 4; ++v)
+                                reinterpret_cast<uint4 *>(bh)[v] = __ldg(reinterpret_cast<const uint4 *>(p.bias + col) + v);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                out[e] = __float2half_rn(__uint_as_float(r[e]) + __half2float(bh[e]));
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) out[e] = __float2half_rn(__uint_as_float(r[e]));
+                        }
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.N + col);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) dst[v] = reinterpret_cast<const uint4 *>(out)[v];
+                    }
+                }
+                tc::fence_before_sync();
+                ptx::mbar_arrive(ptx::smem_addr(acc_empty + abuf));
+                continue;
+            }
+            // ---- a piece of a stream-K tile: store the fp32 partial (first
+            //      piece of this CTA's range in slot 0, last in slot 1), free
+            //      the accumulator and count in. The contributor that counts
+            //      in last finishes the tile after its own loop (below), with
+            //      every warp of the CTA; nobody waits for anybody.
+            const int t = tile - p.dp_waves * (int)gridDim.x;   // stream-K tile index
+            float *mine = p.partials + (int64_t)(2 * (int)blockIdx.x + (si == sg.dp ? 0 : 1)) * kPartialFloats;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t raw[32];
-                tc::ld_32x32b_x32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(abuf * BN + 32 * c), raw);
+                tc::ld_32x32b_x32(t_acc + (uint32_t)(32 * c), raw);
                 tc::ld_wait();
-                uint32_t r[32];
+                if (m < p.M) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = kDequant ? raw[(e & ~7) + unperm(e & 7)] : raw[e];
-                const int col = n0 + 32 * c;
-                if (col < p.N && m < p.M) {
-                    __align__(16) __half out[32];
-                    if (p.bias) {
-                        __align__(16) __half bh[32];
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            reinterpret_cast<uint4 *>(bh)[v] = __ldg(reinterpret_cast<const uint4 *>(p.bias + col) + v);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            out[e] = __float2half_rn(__uint_as_float(r[e]) + __half2float(bh[e]));
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) out[e] = __float2half_rn(__uint_as_float(r[e]));
-                    }
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.N + col);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) dst[v] = reinterpret_cast<const uint4 *>(out)[v];
+                    for (int v = 0; v < 8; ++v)
+                        reinterpret_cast<uint4 *>(mine)[(c * 8 + v) * BM + 32 * q + lane] =
+                            make_uint4(raw[4 * v], raw[4 * v + 1], raw[4 * v + 2], raw[4 * v + 3]);
                 }
             }
             tc::fence_before_sync();
             ptx::mbar_arrive(ptx::smem_addr(acc_empty + abuf));
+            __threadfence();
+            ptx::named_barrier(1, kEpilogueThreads);
+            if (et == 0) {
+                const int cf = sk_cta_of(t * p.kiters, sk_units, p.sk_ctas);
+                const int cl = sk_cta_of(t * p.kiters + p.kiters - 1, sk_units, p.sk_ctas);
+                const unsigned int before = atomicAdd(p.arrive + t, 1u);
+                if (before == (unsigned int)(cl - cf)) fix_tiles[(*fix_count)++] = t;
+            }
         }
     }
+    __syncthreads();
 
+    // ---- finish the stream-K tiles this CTA counted in last for (at most
+    //      two). Every role is done, so the stage ring and the B slots are
+    //      free: the partials of all contributors are brought in with
+    //      asynchronous 16-byte copies (many in flight per thread), summed
+    //      in contributor order, the bias added, rounded once and stored.
+    //      Nothing writes the flags read here after the barrier above.
+    if (*fix_count > 0 && !*abort_flag) {
+        __threadfence();
+        const int sk_units = p.sk_tiles * p.kiters;
+        constexpr int kChunkFloats = BM * 32;              // one 32-column chunk of a partial
+        constexpr int kChunkBytes = kChunkFloats * 4;      // 16 KB
+        constexpr int kFixBytes = C::kBarOff;              // ring + B slots
+        constexpr int kUnitsPerThread = (3 * BM * 4 + kThreads - 1) / kThreads;   // <= 3 chunks a round
+        const uint32_t stage_base = ptx::smem_addr(smem);
+        for (int f = 0; f < *fix_count; ++f) {
+            const int t = fix_tiles[f];
+            const int tile = p.dp_waves * (int)gridDim.x + t;
+            const int m0 = (tile % p.tiles_m) * BM;
+            const int n0 = (tile / p.tiles_m) * BN;
+            const int cf = sk_cta_of(t * p.kiters, sk_units, p.sk_ctas);
+            const int n = sk_cta_of(t * p.kiters + p.kiters - 1, sk_units, p.sk_ctas) - cf + 1;
+            // chunks per round and contributors per batch that fit the free space
+            const int nc = std::max(1, std::min(3, kFixBytes / (n * kChunkBytes)));
+            const int batch = kFixBytes / (nc * kChunkBytes);
+            for (int c0 = 0; c0 < BN / 32; c0 += nc) {
+                const int ncr = std::min(nc, BN / 32 - c0);
+                const int units = ncr * BM * 4;            // (chunk, row, 8-column group)
+                float acc[kUnitsPerThread][8];
+#pragma unroll
+                for (int j = 0; j < kUnitsPerThread; ++j)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
+                for (int b0 = 0; b0 < n; b0 += batch) {
+                    const int nb = std::min(batch, n - b0);
+                    // chunks c0 .. c0 + ncr - 1 of a partial are one contiguous block
+                    const int pieces = ncr * (kChunkBytes / 16);
+                    for (int i = 0; i < nb; ++i) {
+                        const int ci = cf + b0 + i;
+                        const int which = (sk_range_begin(ci, sk_units, p.sk_ctas) / p.kiters == t) ? 0 : 1;
+                        const float *src = p.partials + (int64_t)(2 * ci + which) * kPartialFloats +
+                                           (int64_t)c0 * kChunkFloats;
+                        const uint32_t dst = stage_base + (uint32_t)(i * pieces) * 16;
+                        for (int pc = threadIdx.x; pc < pieces; pc += kThreads)
+                            ptx::cp_async_16(dst + (uint32_t)pc * 16, src + pc * 4);
+                    }
+                    ptx::cp_async_wait_all();
+                    __syncthreads();
+#pragma unroll
+                    for (int j = 0; j < kUnitsPerThread; ++j) {
+                        const int u = threadIdx.x + j * kThreads;
+                        if (u >= units) continue;
+                        const int cc = u / (BM * 4);
+                        const int row = u % BM;
+                        const int grp = (u / BM) % 4;
+                        for (int i = 0; i < nb; ++i) {
+                            const float4 *blk = reinterpret_cast<const float4 *>(smem + (size_t)(i * ncr + cc) * kChunkBytes);
+                            const float4 lo = blk[(2 * grp) * BM + row];
+                            const float4 hi = blk[(2 * grp + 1) * BM + row];
+                            acc[j][0] += lo.x; acc[j][1] += lo.y; acc[j][2] += lo.z; acc[j][3] += lo.w;
+                            acc[j][4] += hi.x; acc[j][5] += hi.y; acc[j][6] += hi.z; acc[j][7] += hi.w;
+                        }
+                    }
+                    __syncthreads();
+                }
+#pragma unroll
+                for (int j = 0; j < kUnitsPerThread; ++j) {
+                    const int u = threadIdx.x + j * kThreads;
+                    if (u >= units) continue;
+                    const int cc = u / (BM * 4);
+                    const int row = u % BM;
+                    const int grp = (u / BM) % 4;
+                    const int m = m0 + row;
+                    const int col = n0 + (c0 + cc) * 32 + grp * 8;
+                    if (m >= p.M || col >= p.N) continue;
+                    float bv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) bv[e] = 0.f;
+                    if (p.bias) {
+                        const uint4 braw = __ldg(reinterpret_cast<const uint4 *>(p.bias + col));
+                        const __half *bh = reinterpret_cast<const __half *>(&braw);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) bv[e] = __half2float(bh[e]);
+                    }
+                    __align__(16) __half out[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        out[e] = __float2half_rn((kDequant ? acc[j][unperm(e)] : acc[j][e]) + bv[e]);
+                    *reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.N + col) = *reinterpret_cast<const uint4 *>(out);
+                }
+            }
+            // every contributor has counted in: the counter is free for the next call
+            if (threadIdx.x == 0) atomicExch(p.arrive + t, 0u);
+        }
+    }
     __syncthreads();
     if (warp == 1) {
         tc::fence_after_sync();
@@ -501,7 +697,19 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream)
     const int tiles_n = (N + BN - 1) / BN;
     const int kiters = (K + BK - 1) / BK;
     const int64_t n_tiles = (int64_t)tiles_m * tiles_n;
-    const int ctas = (int)std::min<int64_t>(n_tiles, li.sms);
+    // Whole waves of tiles go round-robin over one CTA per SM (neighbouring
+    // CTAs share weight tiles in L2). The tiles left over for a last, partial
+    // wave are split along k ("stream-K") between up to one CTA per SM, each
+    // taking at least kMinUnits k-stages, so that the last wave keeps every
+    // SM busy instead of a few.
+    constexpr int kMinUnits = 8;
+    const int dp_waves = (int)(n_tiles / li.sms);
+    const int sk_tiles = (int)(n_tiles - (int64_t)dp_waves * li.sms);
+    const int64_t sk_units = (int64_t)sk_tiles * kiters;
+    const int sk_ctas = sk_tiles == 0 ? 0
+                        : (int)std::min<int64_t>(li.sms, std::max<int64_t>(sk_tiles, sk_units / kMinUnits));
+    const int ctas = dp_waves > 0 ? li.sms : sk_ctas;
+    if (sk_units >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
 
     CUtensorMap tx, tw, ts, tz;
     bool ok = make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.x, K, M, (uint64_t)K * 2, BK, BM,
@@ -532,7 +740,15 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream)
     p.status = device_status_word();
     p.M = M; p.K = K; p.N = N; p.g = g;
     p.tiles_m = tiles_m; p.tiles_n = tiles_n; p.kiters = kiters;
+    p.dp_waves = dp_waves; p.sk_tiles = sk_tiles; p.sk_ctas = sk_ctas;
     p.stage_tx = tx_bytes;
+    if (sk_tiles > 0) {
+        Scratch sc{};
+        if (!get_scratch(stream, (size_t)2 * sk_ctas * kPartialFloats, (size_t)sk_tiles, &sc))
+            return cudaErrorMemoryAllocation;
+        p.partials = sc.partials;
+        p.arrive = sc.counters;
+    }
     prefill_kernel<kDequant, kWhole><<<ctas, kThreads, Cfg<kDequant>::kSmemBytes, stream>>>(tx, tw, ts, tz, p);
     return cudaGetLastError();
 }

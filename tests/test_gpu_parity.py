@@ -97,6 +97,38 @@ def test_ragged_and_edge_shapes(gpu, M, K, N, g, bias):
     check_problem(make_problem(M, K, N, g, bias=bias, seed=M))
 
 
+# Decode on 512-column tiles (N a multiple of 512 and at least 8192): a
+# ragged last k-stage (K % 128 == 64), groups that split a warp's 64 rows
+# (g = 32, 96), both token tiles (M <= 8 and 9..16), with and without bias.
+@pytest.mark.parametrize("M,K,N,g,bias", [
+    (1, 1088, 8192, 32, True),
+    (9, 2112, 8704, 96, False),
+    (16, 4160, 16384, 64, True),
+    (3, 4096, 8192, 128, True),
+    (12, 11008, 12288, 128, True),
+])
+def test_wide_tile_decode(gpu, M, K, N, g, bias):
+    check_problem(make_problem(M, K, N, g, bias=bias, seed=M + 100), full=K * N <= 4160 * 16384)
+
+
+# Prefill with fewer tiles than SMs: every tile's k-stages are split between
+# CTAs ("stream-K") and the partials summed by the last contributor. All
+# outputs are compared, and repeated runs must agree bit for bit (the sum is
+# taken in contributor order, whichever CTA performs it).
+@pytest.mark.parametrize("M,K,N,g,bias", [
+    (40, 4096, 1024, 128, True),
+    (200, 2112, 800, 96, True),     # ragged tile in N, groups that split a stage
+    (129, 1088, 4128, 64, False),   # two token tiles, ragged K and N
+])
+def test_prefill_stream_k(gpu, M, K, N, g, bias):
+    p = make_problem(M, K, N, g, bias=bias, seed=M + 7)
+    check_problem(p, paths=[Path.PREFILL])
+    pg = p.to("cuda")
+    y0 = run_path(pg, Path.PREFILL)
+    for _ in range(3):
+        assert torch.equal(run_path(pg, Path.PREFILL).view(torch.int16), y0.view(torch.int16))
+
+
 # --------------------------------------------------------------------------
 # full-size workloads: sampled rows and column blocks
 # --------------------------------------------------------------------------
@@ -257,8 +289,9 @@ def test_library_cross_check_cublas(gpu):
 
 @pytest.mark.parametrize("M", [1, 16])
 @pytest.mark.parametrize("path", [Path.DECODE, Path.AUTO])
-def test_chained_layers_match_serialised(gpu, M, path):
-    K = N = 2048
+@pytest.mark.parametrize("KN", [2048, 8192])
+def test_chained_layers_match_serialised(gpu, M, path, KN):
+    K = N = KN
     layers = [make_problem(M, K, N, 128, bias=(i == 1), seed=40 + i).to(torch.device("cuda"))
               for i in range(4)]
     x0 = make_activations(M, K, seed=7).cuda()

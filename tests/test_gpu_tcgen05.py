@@ -79,3 +79,25 @@ def test_gemm_f16_argument_rules(gpu):
     assert awq.awq_gemm_f16(A, A, None, B, 4, 64, 40, None) == Status.ERR_INVALID_ARG    # N % 32
     assert awq.awq_gemm_f16(A + 2, A, None, B, 4, 64, 256, None) == Status.ERR_MISALIGNED
     assert awq.awq_gemm_f16(None, None, None, None, 0, 64, 256, None) == Status.OK
+
+
+@pytest.mark.parametrize("M,K,N,bias", [
+    (128, 8192, 512, True),    # 2 tiles split along k between 32 CTAs
+    (300, 2048, 1056, False),  # ragged tiles, pieces of 8 k-stages
+])
+def test_gemm_f16_stream_k_tiles(gpu, M, K, N, bias):
+    """Fewer tiles than SMs: the k-stages of each tile are split between
+    CTAs and the partial sums added by whichever contributor finishes last;
+    the result must not depend on which one that was."""
+    g = torch.Generator().manual_seed(M + K + N + 1)
+    x = torch.randn((M, K), generator=g).half()
+    W = (0.05 * torch.randn((K, N), generator=g)).half()
+    b = (0.1 * torch.randn((N,), generator=g)).half() if bias else None
+    xc, Wc, bc = x.cuda(), W.cuda(), None if b is None else b.cuda()
+    y = gemm(xc, Wc, bc)
+    ref = x.double() @ W.double()
+    if b is not None:
+        ref = ref + b.double()
+    check(y, ref)
+    for _ in range(3):
+        assert torch.equal(gemm(xc, Wc, bc).view(torch.int16), y.view(torch.int16))
