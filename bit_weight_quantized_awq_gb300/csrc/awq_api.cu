@@ -142,7 +142,7 @@ bool path_fits(const Problem &p, awq_path_t path)
 }
 
 // Largest M served by the decode kernel when both fast paths fit.
-constexpr int64_t kDecodeMaxM = 16;
+constexpr int64_t kDecodeMaxM = 32;
 
 awq_path_t auto_path(const Problem &p)
 {

@@ -1,4 +1,4 @@
-// awq_decode.cu -- decode path of the WQLinear forward (small M, 1..16 rows).
+// awq_decode.cu -- decode path of the WQLinear forward (small M, 1..32 rows).
 //
 // Predibase Lorax "AWQ WQLinear" page, Description, forward steps 2-3:
 //   y[m, n] = fp16_rn( sum_k x[m, k] * W[k, n] + bias[n] ),
@@ -28,7 +28,10 @@
 //    16-row chunks): 4 / CW k-groups of 4 CW column warps. Each warp
 //    dequantises in registers and runs the legacy-path tensor-core MMA
 //    m16n8k16 with W as the A operand (16 output columns x 16 k) and the
-//    activations as B (16 k x 8 tokens), fp32 accumulators. Two k-adjacent
+//    activations as B (16 k x 8 tokens), fp32 accumulators; M is padded to
+//    1, 2 or 4 such token tiles, each costing one MMA per A operand (eight
+//    tiles would need more registers than a thread of this 9-warp CTA gets:
+//    three warps share one sub-partition, 168 registers each). Two k-adjacent
 //    weights of one column form one half2 operand register: a byte permute
 //    brings byte b of rows k and k+1 together, one LOP3 masks a nibble into
 //    the fraction of 1024.0 or 64.0, an exact half2 subtract removes the zero
@@ -48,7 +51,7 @@
 //    for the previous kernel; activations, bias, output and scratch are
 //    touched only after that wait.
 //
-// Requirements (else another path serves): 1 <= M <= 16, K % 64 == 0,
+// Requirements (else another path serves): 1 <= M <= 32, K % 64 == 0,
 // N % 32 == 0 (TMA row pitch), g % 16 == 0 with at most 8 groups per 256-row
 // stage (g >= 32), base pointers 16-byte aligned.
 #include <algorithm>
@@ -64,7 +67,7 @@
 namespace awq {
 namespace {
 
-constexpr int kMaxTokens = 16;
+constexpr int kMaxTokens = 32;
 constexpr int kMaxGroupRows = 8;     // group rows one stage may touch
 constexpr int kWBytes = 32768;       // packed weights per stage
 constexpr int kMaxStages = 8;
@@ -87,16 +90,18 @@ struct Geo {
     static constexpr int kKGroups = kConsumerWarps / kColWarps;   // warps down a stage
     static constexpr int kRowsPerWarp = kStageRows / kKGroups;    // 128
     static constexpr int kChunksPerWarp = kRowsPerWarp / 16;
-    static constexpr int kPartialFloats = kMaxTokens * kTileCols;   // also one k-group's fold
     static_assert(kKGroups * kRowsPerWarp == kStageRows, "warps must cover a stage");
 };
-static_assert(Geo<1>::kKGroups == 2 && Geo<1>::kPartialFloats * 4 <= kWBytes, "CW = 1 folds one k-group");
+static_assert(Geo<1>::kKGroups == 2, "CW = 1 folds one k-group");
 static_assert(Geo<2>::kKGroups == 1, "CW = 2 has nothing to fold");
+// A k-group's fp32 sums, 16 MT x 128 floats, fit a CW = 1 slot's weight
+// area (32 KB) for every MT <= 4.
+static_assert(16 * (kMaxTokens / 8) * Geo<1>::kColWarps * 32 * 4 <= kWBytes, "fold buffer fits a slot");
 
 struct DecodeParams {
     const __half *bias;
     __half *y;
-    float *partials;        // [2 * ctas][16][tile columns]
+    float *partials;        // [2 * ctas][8 MT][tile columns]
     unsigned int *arrive;   // [tiles]
     unsigned int *status;
     int M, K, N, g;
@@ -162,6 +167,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     constexpr int kChunksPerWarp = G::kChunksPerWarp;
     constexpr int kRowsPerWarp = G::kRowsPerWarp;
     constexpr int kKGroupThreads = kColWarps * 32;
+    constexpr int kSlotFloats = 8 * MT * kTileCols;   // one partial: 8 MT tokens x the tile
 
     extern __shared__ uint8_t smem_raw[];
     // round up to 1024 bytes by offsetting the shared array itself, so that
@@ -307,18 +313,18 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     // 2 (j % 4) and 2 (j % 4) + 1 -- the k 0..7 and 8..15 halves of its B
     // operand. One ldmatrix.x4 fetches the B operands of a chunk pair for
     // eight tokens: lane L addresses token L % 8, unit 4 * pair + L / 8.
+    // Token tile mt adds 8 kKBlocks rows, which keeps r % 8.
     constexpr int kBlocksPerWarp = kChunksPerWarp / 4;
     static_assert(kChunksPerWarp % 4 == 0, "whole 64-row activation blocks per warp and stage");
-    uint32_t xoff[MT][kBlocksPerWarp][2];
+    constexpr uint32_t kXTokenTile = 8 * kKBlocks * 128;
+    uint32_t xoff[kBlocksPerWarp][2];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+    for (int jb = 0; jb < kBlocksPerWarp; ++jb) {
+        const uint32_t r = (uint32_t)((lane & 7) * kKBlocks + R0 / 64 + jb);
 #pragma unroll
-        for (int jb = 0; jb < kBlocksPerWarp; ++jb) {
-            const uint32_t r = (uint32_t)((8 * mt + (lane & 7)) * kKBlocks + R0 / 64 + jb);
-#pragma unroll
-            for (int pr = 0; pr < 2; ++pr)
-                xoff[mt][jb][pr] = p.x_off + r * 128 + (((uint32_t)(4 * pr + (lane >> 3)) ^ (r & 7)) << 4);
-        }
+        for (int pr = 0; pr < 2; ++pr)
+            xoff[jb][pr] = p.x_off + r * 128 + (((uint32_t)(4 * pr + (lane >> 3)) ^ (r & 7)) << 4);
+    }
     const uint32_t soff = p.s_off + (uint32_t)word * 16;
     const uint32_t zoff = p.z_off + (uint32_t)word * 4;
     // the fp16 exponent patterns OR-ed into the nibbles, read from shared
@@ -415,7 +421,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 if ((j & 1) == 0) {
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt)
-                        ptx::ldmatrix_x4(sbase + xoff[mt][j / 4][(j % 4) / 2], xq[mt]);
+                        ptx::ldmatrix_x4(sbase + xoff[j / 4][(j % 4) / 2] + mt * kXTokenTile, xq[mt]);
                 }
                 uint32_t bf[MT][2];
 #pragma unroll
@@ -493,7 +499,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                         }
                 } else if (!whole && live) {
                     const int which = (tile == first_tile) ? 0 : 1;
-                    float *pslot = p.partials + (int64_t)(2 * c + which) * G::kPartialFloats;
+                    float *pslot = p.partials + (int64_t)(2 * c + which) * kSlotFloats;
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -560,7 +566,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     // does not depend on timing. Only the first contributor may hold the
     // tile in its second slot.
     const int which_cf = (range_begin(cf, p.total, p.ctas) / p.kiters == t) ? 0 : 1;
-    constexpr int kPosPerThread = (kMaxTokens * kTileCols / 4 + kConsumerThreads - 1) / kConsumerThreads;
+    constexpr int kPosPerThread = (8 * MT * kTileCols / 4 + kConsumerThreads - 1) / kConsumerThreads;
     const int n4 = p.M * (kTileCols / 4);   // float4 positions of one partial
     const int per_round = (int)(((uint32_t)S * SB) / (uint32_t)(n4 * 16));
     const uint32_t ring = ptx::smem_addr(smem);
@@ -571,7 +577,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         const int cnt = std::min(per_round, n - r0);
         for (int q = 0; q < cnt; ++q) {
             const int ci = cf + r0 + q;
-            const float *src = p.partials + (int64_t)(2 * ci + (ci == cf ? which_cf : 0)) * G::kPartialFloats;
+            const float *src = p.partials + (int64_t)(2 * ci + (ci == cf ? which_cf : 0)) * kSlotFloats;
 #pragma unroll
             for (int k = 0; k < kPosPerThread; ++k) {
                 const int pos = ctid + k * kConsumerThreads;
@@ -833,7 +839,10 @@ bool decode_supported(int64_t M, int64_t K, int64_t N, int64_t g)
 cudaError_t launch_decode(const Problem &p, cudaStream_t stream)
 {
     if (!decode_supported(p.M, p.K, p.N, p.g)) return cudaErrorInvalidValue;
-    return p.M <= 8 ? dispatch_decode<1>(p, stream) : dispatch_decode<2>(p, stream);
+    // token tiles of 8: one MMA per 16 columns x 16 k and tile
+    if (p.M <= 8) return dispatch_decode<1>(p, stream);
+    if (p.M <= 16) return dispatch_decode<2>(p, stream);
+    return dispatch_decode<4>(p, stream);
 }
 
 } // namespace awq
@@ -851,7 +860,8 @@ namespace {
 
 constexpr int kNoAllocMaxCtas = 160;    // grid cap: partial slots for 160 CTAs
 constexpr int kNoAllocMaxTiles = 8192;  // 256-column tiles: N up to 2,097,152
-constexpr size_t kNoAllocPartialWords = (size_t)2 * kNoAllocMaxCtas * Geo<1>::kPartialFloats;
+constexpr int kNoAllocMaxTokens = 16;   // partial slots hold 16 tokens x 256 columns
+constexpr size_t kNoAllocPartialWords = (size_t)2 * kNoAllocMaxCtas * kNoAllocMaxTokens * Geo<1>::kTileCols;
 constexpr size_t kNoAllocWords = kNoAllocPartialWords + (size_t)kNoAllocMaxTiles;
 
 // fp32 partials (2 slots per CTA) followed by the arrival counter of every
@@ -927,7 +937,7 @@ extern "C" awq_status_t awq_linear_forward_decode_noalloc(
     if (!awq::aligned16_ptr(x) || !awq::aligned16_ptr(qweight) || !awq::aligned16_ptr(qzeros) ||
         !awq::aligned16_ptr(scales) || !awq::aligned16_ptr(y) || (bias && !awq::aligned16_ptr(bias)))
         return AWQ_ERR_MISALIGNED;
-    if (!awq::decode_supported(M, K, N, g)) return AWQ_ERR_INVALID_ARG;
+    if (M > awq::kNoAllocMaxTokens || !awq::decode_supported(M, K, N, g)) return AWQ_ERR_INVALID_ARG;
     if ((N + awq::Geo<1>::kTileCols - 1) / awq::Geo<1>::kTileCols > awq::kNoAllocMaxTiles) return AWQ_ERR_TOO_LARGE;
     uint32_t *scratch = nullptr;
     if (awq::noalloc_scratch_address(&scratch) != cudaSuccess) return AWQ_ERR_CUDA;

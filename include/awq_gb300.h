@@ -161,9 +161,10 @@ awq_status_t awq_gemm_f16(const void *x, const void *W, const void *bias, void *
  * compiled into the library (5,275,648 bytes on every GPU that loads the
  * library, held until the process exits).
  *
- * Arguments, layouts and result: as awq_linear_forward. It serves only the
- * shapes the decode kernel takes (1 <= M <= 16, K % 64 == 0, N % 32 == 0,
- * group_size % 16 == 0 after the -1 rule; else AWQ_ERR_INVALID_ARG) and at
+ * Arguments, layouts and result: as awq_linear_forward. It serves only
+ * shapes the decode kernel takes with at most 16 rows of x (1 <= M <= 16,
+ * K % 64 == 0, N % 32 == 0, group_size % 16 == 0 after the -1 rule; else
+ * AWQ_ERR_INVALID_ARG) and at
  * most 8192 column tiles of 256 (N <= 2,097,152; else AWQ_ERR_TOO_LARGE,
  * returned before anything is enqueued). It uses at most 160 CTAs.
  *

@@ -78,6 +78,19 @@ def test_decode_shapes(gpu, M, K, N):
     check_problem(make_problem(M, K, N, 128, bias=False, seed=0))
 
 
+@pytest.mark.parametrize("M,K,N,g,bias", [
+    (32, 4096, 4096, 128, False),   # four token tiles, split tiles
+    (24, 2112, 1056, 96, True),     # padded tokens, groups that split a warp's rows
+])
+def test_decode_four_token_tiles(gpu, M, K, N, g, bias):
+    check_problem(make_problem(M, K, N, g, bias=bias, seed=M + 50))
+
+
+def test_decode_four_token_tiles_wide(gpu):
+    # 512-column tiles with 32 tokens, sampled rows and column blocks
+    check_problem(make_problem(32, 4096, 32768, 128, bias=True, seed=83), full=False)
+
+
 def test_minimum_n_edge(gpu):
     check_problem(make_problem(1, 4096, 8, -1, bias=True, seed=0))
 
@@ -85,7 +98,8 @@ def test_minimum_n_edge(gpu):
 @pytest.mark.parametrize("M,K,N,g,bias", [
     (5, 1024, 800, 64, True),      # ragged column tile
     (3, 336, 104, 48, False),      # N % 32 != 0, odd group size
-    (17, 768, 288, -1, True),      # M just above the decode limit
+    (17, 768, 288, -1, True),      # four token tiles, 15 of them padding
+    (33, 768, 288, -1, True),      # M just above the decode limit
     (2, 48, 8, 16, False),
     (1, 16, 8, 1, True),           # group size 1
     (7, 1088, 4128, 64, True),     # ragged tile in N and K not a multiple of 128
