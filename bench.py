@@ -45,12 +45,12 @@ METRIC = "AWQ W4A16 GEMM TFLOP/s and weight GB/s vs M (1..8192), % of roofline, 
 # launches), valid only while the kernel sources hash to what was captured.
 NCU_TRAFFIC = {
     "decode-7b": {
-        "bytes_per_launch": 26405909,
+        "bytes_per_launch": 26411115,
         "sources": {
             "bit_weight_quantized_awq_gb300/csrc/awq_decode.cu":
-                "047c5c9b6a0b255bba3da8e0118fe6069d4f92cb2c949d9963afe95db01e5b9e",
+                "d527ef2771be7e23a335bbe4e89eb8a9861b6d2a53532fc6b3350ffe65fd37ee",
             "bit_weight_quantized_awq_gb300/csrc/awq_device.cuh":
-                "0d6b8739c00fe7c14482c2d22a020cbabd9e60a7b0dad4bc1f07068019c49aa4",
+                "3b7d583fc00ea3a961fa897260e5f0245bcdd8b06cb38725fdece027d0787054",
         },
         "summary": "profiles/decode_kernel_decode-7b.md",
     },
