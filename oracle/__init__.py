@@ -18,6 +18,12 @@ against something other than itself):
 * ``forward`` -- fp64 sum over k of x * W16, plus bias; pinned by integer brute
   force on hand cases, the q == z identity, g = -1 vs g = K, scale doubling,
   per-group additivity and a library (numpy fp64 matmul) cross-check.
+* ``pack`` -- the inverse of ``unpack``; pinned by the same hand-packed hex
+  fixtures, a one-hot closed form for every nibble slot, and the two round
+  trips with ``unpack``.
+* ``quantize_rtn`` -- clamp(round_half_even(W / s) + z, 0, 15), packed;
+  pinned by exact grid points (power-of-two scales), hand-computed ties and
+  clamping cases, and quantize(dequant(q)) == q for arbitrary scales.
 """
 from .oracle import (  # noqa: F401
     build,
@@ -25,6 +31,8 @@ from .oracle import (  # noqa: F401
     f16_bits_to_f64,
     resolve_group,
     unpack,
+    pack,
+    quantize_rtn,
     dequant,
     forward,
 )

@@ -315,3 +315,88 @@ int awq_oracle_forward(const uint16_t *x, const int32_t *qweight,
     free(all_rows);
     return rc;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Pack: the inverse of unpack. Code c of row r, column 8j + i goes to bits   */
+/* 4i..4i+3 of int32 j of row r; only the low 4 bits of a code are used.      */
+/* ------------------------------------------------------------------------ */
+
+int awq_oracle_pack(const uint8_t *codes, int64_t rows, int64_t cols, int32_t *packed)
+{
+    if (rows < 0 || cols <= 0 || cols % 8 != 0)
+        return ORACLE_INVALID;
+    int64_t words = cols / 8;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < words; ++j) {
+            uint32_t w = 0;
+            for (int i = 0; i < 8; ++i)
+                w |= (uint32_t)(codes[r * cols + 8 * j + i] & 0xFu) << (4 * i);
+            packed[r * words + j] = (int32_t)w;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Round-to-nearest quantisation with given scales and zero points, the      */
+/* inverse of the dequantisation above:                                      */
+/*   q[k, n] = clamp(round_half_even(W[k, n] / s[k / g, n]) + z[k / g, n],    */
+/*                   0, 15)                                                   */
+/* The quotient of two fp16 values is computed in double. It is exact when   */
+/* it is representable; otherwise it lies at least 2^-12 from any half        */
+/* integer of magnitude below 2^5 (numerator and denominator have 11-bit     */
+/* significands), far more than a double rounding error, so rounding the     */
+/* double quotient decides exactly as rounding the exact quotient would.     */
+/* A NaN quotient (0 / 0) counts as 0. Clamping the quotient to [-64, 64]   */
+/* before rounding (which also handles an infinite quotient) changes no      */
+/* result: after the zero point is added the code is clamped to 0..15.       */
+/* ------------------------------------------------------------------------ */
+
+/* Nearest integer, ties to even, for |y| <= 64 (floor and y - floor exact). */
+static double round_half_even_signed(double y)
+{
+    const double lo = floor(y);
+    const double frac = y - lo;
+    if (frac != 0.5)
+        return frac < 0.5 ? lo : lo + 1.0;
+    return (fmod(lo, 2.0) != 0.0) ? lo + 1.0 : lo;   /* a tie: the even neighbour */
+}
+
+int awq_oracle_quantize_rtn(const uint16_t *W16, const uint16_t *scales, const int32_t *qzeros,
+                            int64_t in_features, int64_t out_features, int64_t group_size,
+                            int32_t *qweight)
+{
+    int64_t K = in_features, N = out_features, g;
+    if (awq_oracle_resolve_group(K, N, group_size, &g) != ORACLE_OK)
+        return ORACLE_INVALID;
+    int64_t G = K / g;
+    uint8_t *q = (uint8_t *)malloc((size_t)(K * N));
+    uint8_t *z = (uint8_t *)malloc((size_t)(G * N));
+    if (!q || !z) {
+        free(q);
+        free(z);
+        return ORACLE_NOMEM;
+    }
+    awq_oracle_unpack(qzeros, G, N, z);
+    for (int64_t k = 0; k < K; ++k) {
+        const int64_t grp = k / g;
+        const uint16_t *srow = scales + grp * N;
+        const uint8_t *zrow = z + grp * N;
+        for (int64_t n = 0; n < N; ++n) {
+            double w = awq_oracle_f16_to_f64(W16[k * N + n]);
+            double t = w / awq_oracle_f16_to_f64(srow[n]);
+            if (isnan(t))
+                t = 0.0;
+            if (t < -64.0)
+                t = -64.0;
+            if (t > 64.0)
+                t = 64.0;
+            int c = (int)round_half_even_signed(t) + (int)zrow[n];
+            q[k * N + n] = (uint8_t)(c < 0 ? 0 : (c > 15 ? 15 : c));
+        }
+    }
+    awq_oracle_pack(q, K, N, qweight);
+    free(q);
+    free(z);
+    return ORACLE_OK;
+}

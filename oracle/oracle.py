@@ -68,6 +68,10 @@ def _load():
         lib.awq_oracle_unpack.argtypes = [_P, _I64, _I64, _P]
         lib.awq_oracle_dequant.restype = ctypes.c_int
         lib.awq_oracle_dequant.argtypes = [_P, _P, _P, _I64, _I64, _I64, _P]
+        lib.awq_oracle_pack.restype = ctypes.c_int
+        lib.awq_oracle_pack.argtypes = [_P, _I64, _I64, _P]
+        lib.awq_oracle_quantize_rtn.restype = ctypes.c_int
+        lib.awq_oracle_quantize_rtn.argtypes = [_P, _P, _P, _I64, _I64, _I64, _P]
         lib.awq_oracle_forward.restype = ctypes.c_int
         lib.awq_oracle_forward.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
                                            _P, _I64, ctypes.c_int, _P]
@@ -129,6 +133,39 @@ def unpack(packed, out_features: int | None = None) -> np.ndarray:
     rc = _load().awq_oracle_unpack(_ptr(packed), rows, n, _ptr(out))
     if rc:
         raise ValueError("oracle rejected the unpack shape")
+    return out
+
+
+def pack(codes) -> np.ndarray:
+    """uint8 codes [R, C] (low 4 bits used) -> int32 [R, C/8]; column 8j + i of
+    a row goes to nibble i of word j."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    rows, cols = codes.shape
+    out = np.empty((rows, cols // 8), dtype=np.int32)
+    rc = _load().awq_oracle_pack(_ptr(codes), rows, cols, _ptr(out))
+    if rc:
+        raise ValueError("oracle rejected the pack shape")
+    return out
+
+
+def quantize_rtn(W, scales, qzeros, group_size: int) -> np.ndarray:
+    """Round-to-nearest codes of fp16 W [K, N] with the given fp16 scales
+    [G, N] and packed zero points [G, N/8], packed: int32 [K, N/8].
+
+    q = clamp(round_half_even(W / s) + z, 0, 15); a NaN quotient counts as 0.
+    """
+    W, scales, qzeros = _u16(W), _u16(scales), _i32(qzeros)
+    K, N = W.shape
+    g = resolve_group(K, N, group_size)
+    if g is None:
+        raise ValueError("oracle rejected the shape")
+    if qzeros.shape != (K // g, N // 8) or scales.shape != (K // g, N):
+        raise ValueError("qzeros/scales shape does not match W and group_size")
+    out = np.empty((K, N // 8), dtype=np.int32)
+    rc = _load().awq_oracle_quantize_rtn(_ptr(W), _ptr(scales), _ptr(qzeros), K, N, group_size,
+                                         _ptr(out))
+    if rc:
+        raise RuntimeError(f"oracle quantize failed ({rc})")
     return out
 
 

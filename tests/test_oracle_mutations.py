@@ -28,6 +28,14 @@ MUTANTS = {
     "ties_away_from_zero": ("return (fmod(r, 2.0) == 0.0) ? r : r + 1.0;", "return r + 1.0;"),
     "weights_transposed_read": ("const uint16_t *wrow = j->W16 + k * N + j->n0;",
                                 "const uint16_t *wrow = j->W16 + (k % N) * N + j->n0;"),
+    "pack_nibble_order_reversed": ("& 0xFu) << (4 * i);", "& 0xFu) << (4 * (7 - i));"),
+    "quantize_ties_round_up": ("return (fmod(lo, 2.0) != 0.0) ? lo + 1.0 : lo;", "return lo + 1.0;"),
+    "quantize_zero_point_dropped": ("int c = (int)round_half_even_signed(t) + (int)zrow[n];",
+                                    "int c = (int)round_half_even_signed(t);"),
+    "quantize_no_clamp": ("q[k * N + n] = (uint8_t)(c < 0 ? 0 : (c > 15 ? 15 : c));",
+                          "q[k * N + n] = (uint8_t)c;"),
+    "quantize_scale_of_group_zero": ("const uint16_t *srow = scales + grp * N;",
+                                     "const uint16_t *srow = scales;"),
 }
 
 

@@ -296,3 +296,88 @@ def test_three_d_input_is_flattened():
     y3 = oracle.forward(x, qw, qz, sc, b, -1)
     y2 = oracle.forward(x.reshape(6, 64), qw, qz, sc, b, -1)
     assert np.array_equal(y3, y2)
+
+
+# --------------------------------------------------------------------------
+# pack (the inverse of unpack): hand-packed fixtures, closed form, round trips
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["hand_8x8.json", "hand_16x16.json"])
+def test_pack_hand_packed(name):
+    d = _load_fixture(name)
+    assert np.array_equal(oracle.pack(d["q"].astype(np.uint8)), d["qweight"])
+    assert np.array_equal(oracle.pack(d["z"].astype(np.uint8)), d["qzeros"])
+
+
+def test_pack_one_hot_closed_form():
+    """Code v at column c of a row is v << 4 (c mod 8) in word c // 8."""
+    for c in range(16):
+        for v in (1, 7, 15):
+            codes = np.zeros((2, 16), dtype=np.uint8)
+            codes[1, c] = v
+            expect = np.zeros((2, 2), dtype=np.uint32)
+            expect[1, c // 8] = v << (4 * (c % 8))
+            assert np.array_equal(oracle.pack(codes).view(np.uint32), expect), (c, v)
+
+
+def test_pack_and_unpack_round_trips():
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 16, size=(37, 96), dtype=np.uint8)
+    assert np.array_equal(oracle.unpack(oracle.pack(codes)), codes)
+    words = rng.integers(0, 2**32, size=(11, 5), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    assert np.array_equal(oracle.pack(oracle.unpack(words)), words)
+    # only the low four bits of a code are used
+    assert np.array_equal(oracle.pack(codes | np.uint8(0xF0)), oracle.pack(codes))
+
+
+# --------------------------------------------------------------------------
+# round-to-nearest quantisation: q = clamp(round_half_even(W / s) + z, 0, 15)
+# --------------------------------------------------------------------------
+
+def test_quantize_recovers_codes_on_exact_grid_points():
+    """Power-of-two scales make W = (q - z) s exact in fp16: q comes back."""
+    rng = np.random.default_rng(4)
+    K, N, g = 64, 48, 16
+    G = K // g
+    q = rng.integers(0, 16, size=(K, N))
+    z = rng.integers(0, 16, size=(G, N))
+    s = np.ldexp(1.0, rng.integers(-10, 2, size=(G, N))).astype(np.float16)
+    Wx = (q - np.repeat(z, g, axis=0)) * np.repeat(s.astype(np.float64), g, axis=0)
+    W = Wx.astype(np.float16)
+    assert np.array_equal(W.astype(np.float64), Wx)   # every point is exact in fp16
+    got = oracle.unpack(oracle.quantize_rtn(W, s, oracle.pack(z.astype(np.uint8)), g))
+    assert np.array_equal(got, q)
+
+
+def test_quantize_hand_cases_ties_and_clamping():
+    """W / s on halves (ties to the even integer), just off halves, and far
+    outside the code range; zero point 8. Expected codes worked by hand from
+    clamp(round_half_even(t) + 8, 0, 15)."""
+    t = [0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 3.375, 3.625, 100.0, -100.0, 7.5, -8.5, 0.0, 6.5, -7.5, -6.5]
+    expect = [8, 10, 10, 8, 6, 6, 11, 12, 15, 0, 15, 0, 8, 14, 0, 2]
+    N = len(t)
+    s = np.full((1, N), 0.25, dtype=np.float16)
+    W = (np.array(t) * 0.25).astype(np.float16).reshape(1, N)
+    assert np.array_equal(W.astype(np.float64).ravel(), np.array(t) * 0.25)
+    z = np.full((1, N), 8, dtype=np.uint8)
+    got = oracle.unpack(oracle.quantize_rtn(W, s, oracle.pack(z), -1))
+    assert got.ravel().tolist() == expect
+
+
+def test_quantize_zero_and_infinite_quotients():
+    """s = 0: 0 / 0 counts as 0 (code = z); x / 0 is infinite and clamps."""
+    W = np.array([[0.0, 1.0, -1.0, 0.0, 0.0, 0.0, 0.0, 0.0]], dtype=np.float16)
+    s = np.array([[0.0, 0.0, 0.0, 1.0, 1.0, 1.0, 1.0, 1.0]], dtype=np.float16)
+    z = np.array([[5, 5, 5, 0, 15, 3, 3, 3]], dtype=np.uint8)
+    got = oracle.unpack(oracle.quantize_rtn(W, s, oracle.pack(z), 1))
+    assert got.ravel().tolist() == [5, 15, 0, 0, 15, 3, 3, 3]
+
+
+@pytest.mark.parametrize("K,N,g", [(256, 64, 32), (128, 40, -1), (96, 16, 48)])
+def test_quantize_inverts_dequant_for_any_scale(K, N, g):
+    """|fp16_rn((q - z) s) / s - (q - z)| <= 15 * 2^-11 < 1/2, so rounding the
+    quotient gives q - z back: quantize(dequant(q)) == q for normal scales."""
+    p = make_problem(1, K, N, g, seed=K + N)
+    W = oracle.dequant(p.qweight.numpy(), p.qzeros.numpy(), p.scales.numpy(), g)
+    back = oracle.quantize_rtn(W, p.scales.numpy(), p.qzeros.numpy(), g)
+    assert np.array_equal(back, p.qweight.numpy())
