@@ -12,6 +12,7 @@ step, more than twice the 129 MB L2), so each call reads its weights cold.
 
     python bench.py [--steps K] [--warmup W] [--impl native|reference]
     python bench.py --sweep --workload all    # per-problem table, every path
+    python bench.py --sweep --workload quantize   # awq_quantize_rtn / awq_pack GB/s
 
 Timing: one CUDA graph per step (its launches each bracketed by external
 event-record nodes); the timed region replays K steps between a barrier +
@@ -520,6 +521,77 @@ def run_sweep(args, device, peaks):
 
 
 # --------------------------------------------------------------------------
+# sweep of the step before the forward: awq_quantize_rtn and awq_pack
+# --------------------------------------------------------------------------
+
+QUANTIZE_SHAPES = DECODE_SHAPES + SWEEP_SHAPES
+
+
+def run_quantize_sweep(args, device, peaks):
+    """Effective GB/s of awq_quantize_rtn (fp16 W + scales + zeros read, packed
+    codes written) and awq_pack (one code byte read, half a byte written) on
+    the 7B and 70B projection shapes, g = 128, back-to-back launches over two
+    copies of the inputs, against the measured HBM copy bandwidth."""
+    import bit_weight_quantized_awq_gb300 as awq
+    awq.load_library()
+    out = open(args.sweep_out, "w") if args.sweep_out else None
+    stream = torch.cuda.Stream(device)
+    h = stream.cuda_stream
+    g = 128
+    for (K, N) in QUANTIZE_SHAPES:
+        G = K // g
+        gen = torch.Generator(device=device).manual_seed(0)
+        sets = []
+        for _ in range(2):
+            W = (torch.randn((K, N), device=device, generator=gen) * 0.02).half()
+            sc = (torch.rand((G, N), device=device, generator=gen) * 9e-3 + 1e-3).half()
+            qz = torch.randint(-2**31, 2**31 - 1, (G, N // 8), dtype=torch.int32, device=device,
+                               generator=gen)
+            codes = torch.randint(0, 16, (K, N), dtype=torch.uint8, device=device, generator=gen)
+            qw = torch.empty((K, N // 8), dtype=torch.int32, device=device)
+            sets.append((W, sc, qz, codes, qw))
+        cases = {
+            "quantize_rtn": (lambda st: awq.awq_quantize_rtn(st[0].data_ptr(), st[1].data_ptr(),
+                                                             st[2].data_ptr(), st[4].data_ptr(),
+                                                             K, N, g, h),
+                             2 * K * N + 2 * G * N + G * N // 2 + K * N // 2),
+            "pack": (lambda st: awq.awq_pack(st[3].data_ptr(), st[4].data_ptr(), K, N, h),
+                     K * N + K * N // 2),
+        }
+        for name, (fn, nbytes) in cases.items():
+            with torch.cuda.stream(stream):
+                for st in sets:
+                    if fn(st) != 0:
+                        raise RuntimeError(f"{name} failed on {(K, N)}")
+            stream.synchronize()
+            reps = 20
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for r in range(reps):
+                    fn(sets[r % 2])
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                graph.replay()
+                stream.synchronize()
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+            torch.cuda.synchronize(device)
+            t = e0.elapsed_time(e1) / 1e3 / reps
+            row = {"workload": "quantize", "kernel": name, "K": K, "N": N, "g": g,
+                   "us": t * 1e6, "gbs": nbytes / t / 1e9, "hbm_frac": nbytes / t / 1e9 / peaks["hbm_gbs"]}
+            print(json.dumps(row), file=sys.stderr, flush=True)
+            if out:
+                out.write(json.dumps(row) + "\n")
+                out.flush()
+            del graph
+        del sets
+        torch.cuda.empty_cache()
+    if out:
+        out.close()
+
+
+# --------------------------------------------------------------------------
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__,
@@ -528,7 +600,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", default="decode-7b", choices=list(WORKLOADS) + ["all"])
+    ap.add_argument("--workload", default="decode-7b", choices=list(WORKLOADS) + ["all", "quantize"])
     ap.add_argument("--path", default="auto", choices=["auto", "generic", "decode", "prefill"])
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-out", default=None)
@@ -552,8 +624,13 @@ def main():
     peaks = load_peaks()
 
     if args.sweep:
-        run_sweep(args, device, peaks)
+        if args.workload == "quantize":
+            run_quantize_sweep(args, device, peaks)
+        else:
+            run_sweep(args, device, peaks)
         return
+    if args.workload == "quantize":
+        ap.error("--workload quantize is a sweep (--sweep)")
 
     problems = WORKLOADS[args.workload]
     r = run_native(args, problems, device)

@@ -19,10 +19,12 @@ from ._binding import (  # noqa: F401
     awq_linear_forward,
     awq_linear_forward_decode_noalloc,
     awq_linear_forward_path,
+    awq_pack,
     awq_path_supported,
+    awq_quantize_rtn,
     awq_select_path,
     awq_shutdown,
     awq_status_string,
     load_library,
 )
-from .layer import AWQLinear, dequant, linear_forward  # noqa: F401
+from .layer import AWQLinear, dequant, linear_forward, pack, quantize_rtn  # noqa: F401

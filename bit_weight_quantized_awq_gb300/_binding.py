@@ -27,6 +27,8 @@ EXPORTED = (
     "awq_shutdown",
     "awq_linear_forward_decode_noalloc",
     "awq_gemm_f16",
+    "awq_pack",
+    "awq_quantize_rtn",
 )
 
 
@@ -91,6 +93,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.awq_linear_forward_decode_noalloc.restype = _INT
         lib.awq_gemm_f16.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P]
         lib.awq_gemm_f16.restype = _INT
+        lib.awq_pack.argtypes = [_P, _P, _I64, _I64, _P]
+        lib.awq_pack.restype = _INT
+        lib.awq_quantize_rtn.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P]
+        lib.awq_quantize_rtn.restype = _INT
         lib.awq_shutdown.argtypes = []
         lib.awq_shutdown.restype = None
         _lib = lib
@@ -124,6 +130,14 @@ def awq_dequant(qweight, qzeros, scales, W, K, N, group_size, stream) -> int:
 
 def awq_gemm_f16(x, W, bias, y, M, K, N, stream) -> int:
     return load_library().awq_gemm_f16(x, W, bias, y, M, K, N, stream)
+
+
+def awq_pack(codes, packed, rows, cols, stream) -> int:
+    return load_library().awq_pack(codes, packed, rows, cols, stream)
+
+
+def awq_quantize_rtn(W, scales, qzeros, qweight, K, N, group_size, stream) -> int:
+    return load_library().awq_quantize_rtn(W, scales, qzeros, qweight, K, N, group_size, stream)
 
 
 def awq_status_string(status) -> str:

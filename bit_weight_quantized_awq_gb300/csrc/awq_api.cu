@@ -240,6 +240,32 @@ awq_status_t awq_dequant(const int32_t *qweight, const int32_t *qzeros, const vo
     return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
 }
 
+awq_status_t awq_pack(const uint8_t *codes, int32_t *packed, int64_t rows, int64_t cols,
+                      awq_stream_t stream)
+{
+    if (rows < 0 || cols <= 0 || cols % 8 != 0) return AWQ_ERR_INVALID_ARG;
+    if (rows == 0) return AWQ_OK;
+    if (!codes || !packed) return AWQ_ERR_INVALID_ARG;
+    if (!aligned16(codes) || !aligned16(packed)) return AWQ_ERR_MISALIGNED;
+    cudaError_t e = awq::launch_pack(codes, packed, rows, cols, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+}
+
+awq_status_t awq_quantize_rtn(const void *W, const void *scales, const int32_t *qzeros,
+                              int32_t *qweight, int64_t K, int64_t N, int64_t group_size,
+                              awq_stream_t stream)
+{
+    int64_t g = 0;
+    awq_status_t st = check_shape(K, N, group_size, &g);
+    if (st != AWQ_OK) return st;
+    if (!W || !scales || !qzeros || !qweight) return AWQ_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(scales) || !aligned16(qzeros) || !aligned16(qweight))
+        return AWQ_ERR_MISALIGNED;
+    Problem p{nullptr, nullptr, qzeros, scales, nullptr, nullptr, 0, K, N, g, K / g};
+    cudaError_t e = awq::launch_quantize(p, W, qweight, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+}
+
 awq_status_t awq_gemm_f16(const void *x, const void *W, const void *bias, void *y, int64_t M,
                           int64_t K, int64_t N, awq_stream_t stream)
 {

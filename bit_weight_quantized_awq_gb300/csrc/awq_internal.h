@@ -42,6 +42,13 @@ bool get_scratch(cudaStream_t stream, size_t partial_floats, size_t n_counters, 
 
 cudaError_t launch_dequant(const Problem &p, void *W, cudaStream_t stream);
 
+// Packing of 4-bit codes (uint8, one per byte) into int32 words, and
+// round-to-nearest quantisation of an fp16 W with the problem's scales and
+// zero points into its qweight.
+cudaError_t launch_pack(const uint8_t *codes, int32_t *packed, int64_t rows, int64_t cols,
+                        cudaStream_t stream);
+cudaError_t launch_quantize(const Problem &p, const void *W, int32_t *qweight, cudaStream_t stream);
+
 cudaError_t launch_generic(const Problem &p, cudaStream_t stream);
 
 // Decode path (small M). supported_* is host-only shape logic.

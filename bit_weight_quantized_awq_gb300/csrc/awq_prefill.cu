@@ -230,9 +230,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     uint8_t *smem = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);   // [kStages] TMA bytes landed
     uint64_t *tfree = full + kStages;       // [kStages] MMAs that read the stage are done
-    uint64_t *bready = tfree + kStages;     // [2] dequantised B slot written
-    uint64_t *bfree = bready + 2;           // [2] MMAs that read the B slot are done
-    uint64_t *acc_full = bfree + 2;         // [2]
+    constexpr int kNB = C::kBSlots > 0 ? C::kBSlots : 1;
+    uint64_t *bready = tfree + kStages;     // [kNB] dequantised B slot written
+    uint64_t *bfree = bready + kNB;         // [kNB] MMAs that read the B slot are done
+    uint64_t *acc_full = bfree + kNB;       // [2]
     uint64_t *acc_empty = acc_full + 2;     // [2]
     uint64_t *drain = acc_empty + 2;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(drain + 1);
@@ -249,9 +250,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             ptx::mbar_init(ptx::smem_addr(full + s), 1);
             ptx::mbar_init(ptx::smem_addr(tfree + s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kNB; ++b) {
             ptx::mbar_init(ptx::smem_addr(bready + b), kDequantThreads);
             ptx::mbar_init(ptx::smem_addr(bfree + b), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(ptx::smem_addr(acc_full + b), 1);
             ptx::mbar_init(ptx::smem_addr(acc_empty + b), kEpilogueThreads);
         }
@@ -334,11 +337,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 const uint32_t d_tmem = tmem_base + (uint32_t)(abuf * BN);
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
-                    const int b = it & 1;
+                    const int b = it % kNB;
                     bool ready = ptx::mbar_wait_bounded(ptx::smem_addr(full + s), (it / kStages) & 1,
                                                         abort_flag, p.status);
                     if (ready && kDequant)
-                        ready = ptx::mbar_wait_bounded(ptx::smem_addr(bready + b), (it >> 1) & 1,
+                        ready = ptx::mbar_wait_bounded(ptx::smem_addr(bready + b), (it / kNB) & 1,
                                                        abort_flag, p.status);
                     if (!ready) {
                         ok = false;
@@ -384,11 +387,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 sg.get(p, si, tile, kb0, kb1);
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
-                    const int b = it & 1;
+                    const int b = it % kNB;
                     bool ready = ptx::mbar_wait_bounded(ptx::smem_addr(full + s), (it / kStages) & 1,
                                                         abort_flag, p.status);
                     if (ready)
-                        ready = ptx::mbar_wait_bounded(ptx::smem_addr(bfree + b), ((it >> 1) & 1) ^ 1,
+                        ready = ptx::mbar_wait_bounded(ptx::smem_addr(bfree + b), ((it / kNB) & 1) ^ 1,
                                                        abort_flag, p.status);
                     if (!ready) {
                         ok = false;

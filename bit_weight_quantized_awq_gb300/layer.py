@@ -12,7 +12,8 @@ from __future__ import annotations
 
 import torch
 
-from ._binding import AWQError, Path, Status, awq_dequant, awq_linear_forward_path
+from ._binding import (AWQError, Path, Status, awq_dequant, awq_linear_forward_path, awq_pack,
+                       awq_quantize_rtn)
 
 
 def _ptr(t):
@@ -80,6 +81,48 @@ def dequant(qweight: torch.Tensor, qzeros: torch.Tensor, scales: torch.Tensor,
                      _stream(dev))
     if st != Status.OK:
         raise AWQError(st, "awq_dequant")
+    return out
+
+
+def pack(codes: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """uint8 codes [R, C] (low 4 bits used) -> int32 [R, C/8], column 8j + i of
+    a row in nibble i of word j: the layout of qweight and qzeros."""
+    dev = codes.device
+    if dev.type != "cuda":
+        raise ValueError("the AWQ library runs on CUDA tensors only")
+    _check(codes, "codes", torch.uint8, dev)
+    if codes.dim() != 2:
+        raise ValueError("codes must be 2-D [rows, cols]")
+    R, C = codes.shape
+    if out is None:
+        out = torch.empty((R, C // 8), dtype=torch.int32, device=dev)
+    else:
+        _check(out, "out", torch.int32, dev)
+    st = awq_pack(_ptr(codes), _ptr(out), R, C, _stream(dev))
+    if st != Status.OK:
+        raise AWQError(st, "awq_pack")
+    return out
+
+
+def quantize_rtn(W: torch.Tensor, scales: torch.Tensor, qzeros: torch.Tensor, group_size: int,
+                 out: torch.Tensor | None = None) -> torch.Tensor:
+    """qweight int32 [K, N/8]: q = clamp(round_half_even(W / s) + z, 0, 15) per
+    group, packed -- the inverse of ``dequant`` for the given scales and zeros."""
+    dev = W.device
+    if dev.type != "cuda":
+        raise ValueError("the AWQ library runs on CUDA tensors only")
+    _check(W, "W", torch.float16, dev)
+    _check(scales, "scales", torch.float16, dev)
+    _check(qzeros, "qzeros", torch.int32, dev)
+    K, N = W.shape
+    if out is None:
+        out = torch.empty((K, N // 8), dtype=torch.int32, device=dev)
+    else:
+        _check(out, "out", torch.int32, dev)
+    st = awq_quantize_rtn(_ptr(W), _ptr(scales), _ptr(qzeros), _ptr(out), K, N, group_size,
+                          _stream(dev))
+    if st != Status.OK:
+        raise AWQError(st, "awq_quantize_rtn")
     return out
 
 

@@ -133,6 +133,41 @@ awq_status_t awq_dequant(const int32_t *qweight, const int32_t *qzeros,
                          int64_t group_size, awq_stream_t stream);
 
 /*
+ * awq_pack -- packs 4-bit codes into the layer's int32 format, the inverse of
+ * the unpacking every forward call does (I/O Contract of the WQLinear page:
+ * eight 4-bit values per int32; the order is this library's reading):
+ *   packed[r, j] = sum_i (codes[r, 8 j + i] & 0xF) << (4 i),   i = 0..7.
+ *   codes   uint8 [rows, cols], one code per byte (read; only the low 4 bits
+ *           of each byte are used)
+ *   packed  int32 [rows, cols / 8]                     (written)
+ * Serves qweight (rows = K, cols = N) and qzeros (rows = G). Requires
+ * rows >= 0, cols > 0 and cols % 8 == 0 (AWQ_ERR_INVALID_ARG otherwise);
+ * rows == 0 is a no-op (pointers may be NULL then); both base pointers
+ * 16-byte aligned (AWQ_ERR_MISALIGNED).
+ */
+awq_status_t awq_pack(const uint8_t *codes, int32_t *packed, int64_t rows, int64_t cols,
+                      awq_stream_t stream);
+
+/*
+ * awq_quantize_rtn -- round-to-nearest quantisation of an fp16 weight with
+ * given per-group scales and zero points, packed; the inverse of the
+ * dequantisation W = (q - z) * s (Overview of the WQLinear page: group-wise
+ * scaling):
+ *   q[k, n] = clamp(round_half_even(W[k, n] / s[k / g, n]) + z[k / g, n], 0, 15)
+ *   W       fp16 [K, N]                   (read)
+ *   scales  fp16 [G, N], qzeros int32 [G, N / 8]   (read)
+ *   qweight int32 [K, N / 8]              (written)
+ * The quotient of two fp16 values is rounded as if exact (it is formed in
+ * fp32, which decides every rounding the same way); a NaN quotient (0 / 0)
+ * counts as 0, an infinite one clamps. For any normal nonzero scale,
+ * awq_quantize_rtn(awq_dequant(q)) returns q. Shape and pointer rules as
+ * awq_dequant.
+ */
+awq_status_t awq_quantize_rtn(const void *W, const void *scales, const int32_t *qzeros,
+                              int32_t *qweight, int64_t K, int64_t N, int64_t group_size,
+                              awq_stream_t stream);
+
+/*
  * awq_gemm_f16 -- y[M, N] = fp16_rn(x[M, K] . W[K, N] + bias[N]) for an
  * already dequantised fp16 W (row-major [K, N], e.g. from awq_dequant), on the
  * same tcgen05 tensor-core pipeline as the prefill path of awq_linear_forward

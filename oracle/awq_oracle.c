@@ -343,8 +343,8 @@ int awq_oracle_pack(const uint8_t *codes, int64_t rows, int64_t cols, int32_t *p
 /*   q[k, n] = clamp(round_half_even(W[k, n] / s[k / g, n]) + z[k / g, n],    */
 /*                   0, 15)                                                   */
 /* The quotient of two fp16 values is computed in double. It is exact when   */
-/* it is representable; otherwise it lies at least 2^-12 from any half        */
-/* integer of magnitude below 2^5 (numerator and denominator have 11-bit     */
+/* it is representable; otherwise it lies at least 2^-13 from any half        */
+/* integer of magnitude up to 64 (numerator and denominator have 11-bit      */
 /* significands), far more than a double rounding error, so rounding the     */
 /* double quotient decides exactly as rounding the exact quotient would.     */
 /* A NaN quotient (0 / 0) counts as 0. Clamping the quotient to [-64, 64]   */

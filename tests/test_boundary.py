@@ -97,6 +97,29 @@ def test_dequant_null_and_misaligned(lib):
     assert awq.awq_dequant(A, A, A, B + 8, 256, 64, 128, None) == Status.ERR_MISALIGNED
 
 
+def test_pack_argument_rules(lib):
+    assert awq.awq_pack(A, B, 4, 12, None) == Status.ERR_INVALID_ARG     # cols % 8
+    assert awq.awq_pack(A, B, 4, 0, None) == Status.ERR_INVALID_ARG
+    assert awq.awq_pack(A, B, -1, 8, None) == Status.ERR_INVALID_ARG
+    assert awq.awq_pack(None, B, 4, 8, None) == Status.ERR_INVALID_ARG
+    assert awq.awq_pack(A + 8, B, 4, 8, None) == Status.ERR_MISALIGNED
+    assert awq.awq_pack(A, B + 4, 4, 8, None) == Status.ERR_MISALIGNED
+    assert awq.awq_pack(None, None, 0, 8, None) == Status.OK            # nothing to do
+
+
+@pytest.mark.parametrize("kw", [dict(N=12), dict(g=0), dict(g=-3), dict(K=256, g=96), dict(K=0)])
+def test_quantize_invalid(lib, kw):
+    K, N, g = kw.get("K", 256), kw.get("N", 64), kw.get("g", 128)
+    assert awq.awq_quantize_rtn(A, A, A, B, K, N, g, None) == Status.ERR_INVALID_ARG
+
+
+def test_quantize_null_and_misaligned(lib):
+    assert awq.awq_quantize_rtn(None, A, A, B, 256, 64, 128, None) == Status.ERR_INVALID_ARG
+    assert awq.awq_quantize_rtn(A, A, A, None, 256, 64, 128, None) == Status.ERR_INVALID_ARG
+    assert awq.awq_quantize_rtn(A + 2, A, A, B, 256, 64, 128, None) == Status.ERR_MISALIGNED
+    assert awq.awq_quantize_rtn(A, A, A + 4, B, 256, 64, 128, None) == Status.ERR_MISALIGNED
+
+
 def test_path_support_rules(lib):
     # the generic kernel takes every valid shape, nothing takes an invalid one
     for (M, K, N, g) in [(1, 4096, 8, -1), (3, 48, 104, 16), (5, 336, 800, 48), (1, 1, 8, 1)]:
