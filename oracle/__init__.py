@@ -18,6 +18,11 @@ against something other than itself):
 * ``forward`` -- fp64 sum over k of x * W16, plus bias; pinned by integer brute
   force on hand cases, the q == z identity, g = -1 vs g = K, scale doubling,
   per-group additivity and a library (numpy fp64 matmul) cross-check.
+* ``dequant_gidx`` / ``forward_gidx`` -- the same with the group of input
+  row k read from a table g_idx[k] ("act-order" grouping); pinned by equality
+  with ``dequant`` / ``forward`` when g_idx[k] = k // g, by equivariance under
+  a permutation of the rows, and by a constant table (one group) against
+  ``dequant`` with g = K on that group's scales and zeros.
 * ``pack`` -- the inverse of ``unpack``; pinned by the same hand-packed hex
   fixtures, a one-hot closed form for every nibble slot, and the two round
   trips with ``unpack``.
@@ -35,4 +40,6 @@ from .oracle import (  # noqa: F401
     quantize_rtn,
     dequant,
     forward,
+    dequant_gidx,
+    forward_gidx,
 )

@@ -245,18 +245,14 @@ static void *fwd_worker(void *arg)
     return NULL;
 }
 
-/* x: fp16 bits [M, K]; rows: which rows of x to evaluate (NULL = all M, in
- * order); y: fp64 [n_rows, N]. threads <= 0 means one thread. */
-int awq_oracle_forward(const uint16_t *x, const int32_t *qweight,
-                       const int32_t *qzeros, const uint16_t *scales,
-                       const uint16_t *bias, int64_t M, int64_t in_features,
-                       int64_t out_features, int64_t group_size,
-                       const int64_t *rows, int64_t n_rows, int threads,
-                       double *y)
+/* The matmul and bias add of the forward, given the fp16 weights W16 [K, N]:
+ * y[r, n] = sum_k x[rows[r], k] * W16[k, n] + bias[n] in fp64. rows: which
+ * rows of x to evaluate (NULL = all M, in order); y: fp64 [n_rows, N].
+ * threads <= 0 means one thread. */
+static int forward_from_w16(const uint16_t *x, const uint16_t *W16, const uint16_t *bias,
+                            int64_t M, int64_t K, int64_t N, const int64_t *rows,
+                            int64_t n_rows, int threads, double *y)
 {
-    int64_t K = in_features, N = out_features, g;
-    if (M < 0 || awq_oracle_resolve_group(K, N, group_size, &g) != ORACLE_OK)
-        return ORACLE_INVALID;
     int64_t *all_rows = NULL;
     if (!rows) {
         n_rows = M;
@@ -273,17 +269,7 @@ int awq_oracle_forward(const uint16_t *x, const int32_t *qweight,
             return ORACLE_INVALID;
         }
     }
-    uint16_t *W16 = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(K * N));
-    if (!W16) {
-        free(all_rows);
-        return ORACLE_NOMEM;
-    }
-    int rc = awq_oracle_dequant(qweight, qzeros, scales, K, N, group_size, W16);
-    if (rc != ORACLE_OK) {
-        free(W16);
-        free(all_rows);
-        return rc;
-    }
+    int rc = ORACLE_OK;
     if (threads < 1)
         threads = 1;
     if (threads > 256)
@@ -311,8 +297,88 @@ int awq_oracle_forward(const uint16_t *x, const int32_t *qweight,
                 rc = ORACLE_NOMEM;
         }
     }
-    free(W16);
     free(all_rows);
+    return rc;
+}
+
+/* x: fp16 bits [M, K]; rows: which rows of x to evaluate (NULL = all M, in
+ * order); y: fp64 [n_rows, N]. threads <= 0 means one thread. */
+int awq_oracle_forward(const uint16_t *x, const int32_t *qweight,
+                       const int32_t *qzeros, const uint16_t *scales,
+                       const uint16_t *bias, int64_t M, int64_t in_features,
+                       int64_t out_features, int64_t group_size,
+                       const int64_t *rows, int64_t n_rows, int threads,
+                       double *y)
+{
+    int64_t K = in_features, N = out_features, g;
+    if (M < 0 || awq_oracle_resolve_group(K, N, group_size, &g) != ORACLE_OK)
+        return ORACLE_INVALID;
+    uint16_t *W16 = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(K * N));
+    if (!W16)
+        return ORACLE_NOMEM;
+    int rc = awq_oracle_dequant(qweight, qzeros, scales, K, N, group_size, W16);
+    if (rc == ORACLE_OK)
+        rc = forward_from_w16(x, W16, bias, M, K, N, rows, n_rows, threads, y);
+    free(W16);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Grouping by table (the "g_idx" variant): the group of input row k is       */
+/* g_idx[k] instead of k / group_size, with G groups of scales and zeros:     */
+/*   W16[k, n] = fp16_rn((q[k, n] - z[g_idx[k], n]) * scale[g_idx[k], n]).     */
+/* Every g_idx[k] must lie in [0, G).                                          */
+/* ------------------------------------------------------------------------ */
+
+int awq_oracle_dequant_gidx(const int32_t *qweight, const int32_t *qzeros,
+                            const uint16_t *scales, const int32_t *g_idx,
+                            int64_t in_features, int64_t out_features, int64_t groups,
+                            uint16_t *W16)
+{
+    int64_t K = in_features, N = out_features, G = groups;
+    if (K <= 0 || N <= 0 || N % 8 != 0 || G <= 0)
+        return ORACLE_INVALID;
+    for (int64_t k = 0; k < K; ++k)
+        if (g_idx[k] < 0 || g_idx[k] >= G)
+            return ORACLE_INVALID;
+    uint8_t *q = (uint8_t *)malloc((size_t)(K * N));
+    uint8_t *z = (uint8_t *)malloc((size_t)(G * N));
+    if (!q || !z) {
+        free(q);
+        free(z);
+        return ORACLE_NOMEM;
+    }
+    awq_oracle_unpack(qweight, K, N, q);
+    awq_oracle_unpack(qzeros, G, N, z);
+    for (int64_t k = 0; k < K; ++k) {
+        const int64_t row_group = g_idx[k];
+        for (int64_t n = 0; n < N; ++n) {
+            int diff = (int)q[k * N + n] - (int)z[row_group * N + n];
+            double sc = awq_oracle_f16_to_f64(scales[row_group * N + n]);
+            W16[k * N + n] = awq_oracle_f64_to_f16((double)diff * sc);
+        }
+    }
+    free(q);
+    free(z);
+    return ORACLE_OK;
+}
+
+int awq_oracle_forward_gidx(const uint16_t *x, const int32_t *qweight,
+                            const int32_t *qzeros, const uint16_t *scales,
+                            const int32_t *g_idx, const uint16_t *bias, int64_t M,
+                            int64_t in_features, int64_t out_features, int64_t groups,
+                            const int64_t *rows, int64_t n_rows, int threads, double *y)
+{
+    int64_t K = in_features, N = out_features;
+    if (M < 0 || K <= 0 || N <= 0)
+        return ORACLE_INVALID;
+    uint16_t *W16 = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(K * N));
+    if (!W16)
+        return ORACLE_NOMEM;
+    int rc = awq_oracle_dequant_gidx(qweight, qzeros, scales, g_idx, K, N, groups, W16);
+    if (rc == ORACLE_OK)
+        rc = forward_from_w16(x, W16, bias, M, K, N, rows, n_rows, threads, y);
+    free(W16);
     return rc;
 }
 

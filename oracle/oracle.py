@@ -68,6 +68,11 @@ def _load():
         lib.awq_oracle_unpack.argtypes = [_P, _I64, _I64, _P]
         lib.awq_oracle_dequant.restype = ctypes.c_int
         lib.awq_oracle_dequant.argtypes = [_P, _P, _P, _I64, _I64, _I64, _P]
+        lib.awq_oracle_dequant_gidx.restype = ctypes.c_int
+        lib.awq_oracle_dequant_gidx.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P]
+        lib.awq_oracle_forward_gidx.restype = ctypes.c_int
+        lib.awq_oracle_forward_gidx.argtypes = [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
+                                                _P, _I64, ctypes.c_int, _P]
         lib.awq_oracle_pack.restype = ctypes.c_int
         lib.awq_oracle_pack.argtypes = [_P, _I64, _I64, _P]
         lib.awq_oracle_quantize_rtn.restype = ctypes.c_int
@@ -221,4 +226,53 @@ def forward(x, qweight, qzeros, scales, bias, group_size: int, rows=None,
                                     rows_a.size, int(threads), _ptr(y))
     if rc:
         raise RuntimeError(f"oracle forward failed ({rc})")
+    return y
+
+
+def _gidx(g_idx, K):
+    g_idx = np.ascontiguousarray(g_idx, dtype=np.int32)
+    if g_idx.shape != (K,):
+        raise ValueError("g_idx must have shape [K]")
+    return g_idx
+
+
+def dequant_gidx(qweight, qzeros, scales, g_idx) -> np.ndarray:
+    """W16 bit patterns [K, N] with the group of row k taken from g_idx[k]."""
+    qweight, qzeros, scales = _i32(qweight), _i32(qzeros), _u16(scales)
+    K, words = qweight.shape
+    N = 8 * words
+    G = scales.shape[0]
+    g_idx = _gidx(g_idx, K)
+    if qzeros.shape != (G, words) or scales.shape != (G, N):
+        raise ValueError("qzeros/scales shape does not match qweight")
+    out = np.empty((K, N), dtype=np.uint16)
+    rc = _load().awq_oracle_dequant_gidx(_ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(g_idx),
+                                         K, N, G, _ptr(out))
+    if rc:
+        raise ValueError(f"oracle rejected the g_idx problem ({rc})")
+    return out
+
+
+def forward_gidx(x, qweight, qzeros, scales, g_idx, bias, rows=None,
+                 threads: int | None = None) -> np.ndarray:
+    """fp64 y with the group of input row k taken from g_idx[k]."""
+    x = _u16(x)
+    x = x.reshape(-1, x.shape[-1])
+    qweight, qzeros, scales = _i32(qweight), _i32(qzeros), _u16(scales)
+    bias = None if bias is None else _u16(bias)
+    M, K = x.shape
+    N = 8 * qweight.shape[1]
+    G = scales.shape[0]
+    g_idx = _gidx(g_idx, K)
+    if qweight.shape[0] != K or qzeros.shape != (G, N // 8) or scales.shape != (G, N):
+        raise ValueError("shapes do not match")
+    rows_a = np.arange(M, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    y = np.empty((rows_a.size, N), dtype=np.float64)
+    rc = _load().awq_oracle_forward_gidx(_ptr(x), _ptr(qweight), _ptr(qzeros), _ptr(scales),
+                                         _ptr(g_idx), _ptr(bias), M, K, N, G, _ptr(rows_a),
+                                         rows_a.size, int(threads), _ptr(y))
+    if rc:
+        raise RuntimeError(f"oracle forward_gidx failed ({rc})")
     return y

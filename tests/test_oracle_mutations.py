@@ -36,6 +36,9 @@ MUTANTS = {
                           "q[k * N + n] = (uint8_t)c;"),
     "quantize_scale_of_group_zero": ("const uint16_t *srow = scales + grp * N;",
                                      "const uint16_t *srow = scales;"),
+    "gidx_table_ignored": ("const int64_t row_group = g_idx[k];", "const int64_t row_group = k % G;"),
+    "gidx_zero_of_wrong_row": ("int diff = (int)q[k * N + n] - (int)z[row_group * N + n];",
+                               "int diff = (int)q[k * N + n] - (int)z[(k % G) * N + n];"),
 }
 
 

@@ -381,3 +381,63 @@ def test_quantize_inverts_dequant_for_any_scale(K, N, g):
     W = oracle.dequant(p.qweight.numpy(), p.qzeros.numpy(), p.scales.numpy(), g)
     back = oracle.quantize_rtn(W, p.scales.numpy(), p.qzeros.numpy(), g)
     assert np.array_equal(back, p.qweight.numpy())
+
+
+# --------------------------------------------------------------------------
+# grouping by table (g_idx): the group of input row k is g_idx[k]
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("K,N,g", [(256, 64, 32), (96, 16, 48), (64, 40, -1)])
+def test_gidx_with_floor_table_equals_grouped(K, N, g):
+    """g_idx[k] = k // g reproduces the grouped dequant and forward exactly."""
+    p = make_problem(5, K, N, g, bias=True, seed=K + 1)
+    gg = K if g == -1 else g
+    table = (np.arange(K) // gg).astype(np.int32)
+    qw, qz, sc = p.qweight.numpy(), p.qzeros.numpy(), p.scales.numpy()
+    assert np.array_equal(oracle.dequant_gidx(qw, qz, sc, table), oracle.dequant(qw, qz, sc, g))
+    y1 = oracle.forward_gidx(p.x.numpy(), qw, qz, sc, table, p.bias.numpy())
+    y2 = oracle.forward(p.x.numpy(), qw, qz, sc, p.bias.numpy(), g)
+    assert np.array_equal(y1, y2)
+
+
+def test_gidx_follows_a_permutation_of_the_rows():
+    """Permuting the rows of qweight together with g_idx permutes the rows of
+    W16; permuting x's columns the same way leaves y unchanged."""
+    K, N, G = 96, 32, 6
+    p = make_problem(3, K, N, K // G * 1, bias=False, seed=7)
+    rng = np.random.default_rng(11)
+    table = rng.integers(0, G, size=K).astype(np.int32)
+    qw, qz, sc = p.qweight.numpy(), p.qzeros.numpy(), p.scales.numpy()
+    assert qz.shape[0] == G
+    perm = rng.permutation(K)
+    W = oracle.dequant_gidx(qw, qz, sc, table)
+    Wp = oracle.dequant_gidx(np.ascontiguousarray(qw[perm]), qz, sc, table[perm])
+    assert np.array_equal(Wp, W[perm])
+    x = p.x.numpy()
+    y = oracle.forward_gidx(x, qw, qz, sc, table, None)
+    yp = oracle.forward_gidx(np.ascontiguousarray(x[:, perm]), np.ascontiguousarray(qw[perm]), qz, sc,
+                             table[perm], None)
+    assert np.allclose(yp, y, rtol=1e-12, atol=1e-12)
+
+
+def test_gidx_constant_table_is_one_group():
+    """Every row in group c: the dequant of a single group (g = K) with group
+    c's scales and zero points."""
+    K, N, G = 64, 24, 4
+    p = make_problem(1, K, N, K // G, seed=13)
+    qw, qz, sc = p.qweight.numpy(), p.qzeros.numpy(), p.scales.numpy()
+    for c in range(G):
+        table = np.full(K, c, dtype=np.int32)
+        expect = oracle.dequant(qw, np.ascontiguousarray(qz[c:c + 1]), np.ascontiguousarray(sc[c:c + 1]), -1)
+        assert np.array_equal(oracle.dequant_gidx(qw, qz, sc, table), expect), c
+
+
+def test_gidx_rejects_out_of_range_groups():
+    p = make_problem(1, 32, 16, 8, seed=3)
+    table = np.zeros(32, dtype=np.int32)
+    table[5] = 4                      # G = 4 groups: 0..3
+    with pytest.raises(ValueError):
+        oracle.dequant_gidx(p.qweight.numpy(), p.qzeros.numpy(), p.scales.numpy(), table)
+    table[5] = -1
+    with pytest.raises(ValueError):
+        oracle.dequant_gidx(p.qweight.numpy(), p.qzeros.numpy(), p.scales.numpy(), table)
