@@ -13,6 +13,7 @@ step, more than twice the 129 MB L2), so each call reads its weights cold.
     python bench.py [--steps K] [--warmup W] [--impl native|reference]
     python bench.py --sweep --workload all    # per-problem table, every path
     python bench.py --sweep --workload quantize   # awq_quantize_rtn / awq_pack GB/s
+    python bench.py --sweep --workload gidx       # awq_linear_forward_gidx TFLOP/s
 
 Timing: one CUDA graph per step (its launches each bracketed by external
 event-record nodes); the timed region replays K steps between a barrier +
@@ -591,6 +592,65 @@ def run_quantize_sweep(args, device, peaks):
         out.close()
 
 
+def run_gidx_sweep(args, device, peaks):
+    """awq_linear_forward_gidx (act-order table: each group holds 128 rows,
+    scattered by a permutation) on 7B-class shapes: TFLOP/s and the binding
+    roofline fraction, back-to-back launches over two weight copies."""
+    import bit_weight_quantized_awq_gb300 as awq
+    awq.load_library()
+    out = open(args.sweep_out, "w") if args.sweep_out else None
+    stream = torch.cuda.Stream(device)
+    h = stream.cuda_stream
+    for (K, N) in [(4096, 12288), (11008, 4096)]:
+        G = K // 128
+        for M in (1, 16, 512, 2048, 8192):
+            gen = torch.Generator(device=device).manual_seed(0)
+            sets = []
+            for _ in range(2):
+                qw = torch.randint(-2**31, 2**31 - 1, (K, N // 8), dtype=torch.int32, device=device, generator=gen)
+                qz = torch.randint(-2**31, 2**31 - 1, (G, N // 8), dtype=torch.int32, device=device, generator=gen)
+                sc = (torch.rand((G, N), device=device, generator=gen) * 9e-3 + 1e-3).half()
+                perm = torch.randperm(K, device=device, generator=gen)
+                gi = (torch.arange(K, device=device) // 128)[perm].to(torch.int32).contiguous()
+                sets.append((qw, qz, sc, gi))
+            x = torch.randn((M, K), device=device, generator=gen).half()
+            y = torch.empty((M, N), device=device, dtype=torch.float16)
+            fn = lambda st: awq.awq_linear_forward_gidx(x.data_ptr(), st[0].data_ptr(), st[1].data_ptr(),
+                                                        st[2].data_ptr(), st[3].data_ptr(), None,
+                                                        y.data_ptr(), M, K, N, G, h)
+            with torch.cuda.stream(stream):
+                for st in sets:
+                    if fn(st) != 0:
+                        raise RuntimeError(f"gidx forward failed on {(M, K, N)}")
+            stream.synchronize()
+            reps = max(3, min(50, int(2e-3 / max(1e-7, flops(M, K, N) / 1e15))))
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for r in range(reps):
+                    fn(sets[r % 2])
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                graph.replay()
+                stream.synchronize()
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+            torch.cuda.synchronize(device)
+            t = e0.elapsed_time(e1) / 1e3 / reps
+            row = {"workload": "gidx", "M": M, "K": K, "N": N, "G": G, "us": t * 1e6,
+                   "tflops": flops(M, K, N) / t / 1e12,
+                   "tc_frac": flops(M, K, N) / t / 1e12 / peaks["bf16_tflops"],
+                   "hbm_frac": algo_bytes(M, K, N, 128, False) / t / 1e9 / peaks["hbm_gbs"]}
+            print(json.dumps(row), file=sys.stderr, flush=True)
+            if out:
+                out.write(json.dumps(row) + "\n")
+                out.flush()
+            del graph, sets
+            torch.cuda.empty_cache()
+    if out:
+        out.close()
+
+
 # --------------------------------------------------------------------------
 
 def main():
@@ -600,7 +660,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", default="decode-7b", choices=list(WORKLOADS) + ["all", "quantize"])
+    ap.add_argument("--workload", default="decode-7b", choices=list(WORKLOADS) + ["all", "quantize", "gidx"])
     ap.add_argument("--path", default="auto", choices=["auto", "generic", "decode", "prefill"])
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-out", default=None)
@@ -626,11 +686,13 @@ def main():
     if args.sweep:
         if args.workload == "quantize":
             run_quantize_sweep(args, device, peaks)
+        elif args.workload == "gidx":
+            run_gidx_sweep(args, device, peaks)
         else:
             run_sweep(args, device, peaks)
         return
-    if args.workload == "quantize":
-        ap.error("--workload quantize is a sweep (--sweep)")
+    if args.workload in ("quantize", "gidx"):
+        ap.error(f"--workload {args.workload} is a sweep (--sweep)")
 
     problems = WORKLOADS[args.workload]
     r = run_native(args, problems, device)

@@ -14,10 +14,12 @@ from ._binding import (  # noqa: F401
     Path,
     Status,
     awq_dequant,
+    awq_dequant_gidx,
     awq_gemm_f16,
     awq_last_device_status,
     awq_linear_forward,
     awq_linear_forward_decode_noalloc,
+    awq_linear_forward_gidx,
     awq_linear_forward_path,
     awq_pack,
     awq_path_supported,
@@ -27,4 +29,5 @@ from ._binding import (  # noqa: F401
     awq_status_string,
     load_library,
 )
-from .layer import AWQLinear, dequant, linear_forward, pack, quantize_rtn  # noqa: F401
+from .layer import (AWQLinear, dequant, dequant_gidx, linear_forward, linear_forward_gidx,  # noqa: F401
+                    pack, quantize_rtn)

@@ -29,6 +29,8 @@ EXPORTED = (
     "awq_gemm_f16",
     "awq_pack",
     "awq_quantize_rtn",
+    "awq_dequant_gidx",
+    "awq_linear_forward_gidx",
 )
 
 
@@ -93,6 +95,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.awq_linear_forward_decode_noalloc.restype = _INT
         lib.awq_gemm_f16.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P]
         lib.awq_gemm_f16.restype = _INT
+        lib.awq_dequant_gidx.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]
+        lib.awq_dequant_gidx.restype = _INT
+        lib.awq_linear_forward_gidx.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]
+        lib.awq_linear_forward_gidx.restype = _INT
         lib.awq_pack.argtypes = [_P, _P, _I64, _I64, _P]
         lib.awq_pack.restype = _INT
         lib.awq_quantize_rtn.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P]
@@ -130,6 +136,15 @@ def awq_dequant(qweight, qzeros, scales, W, K, N, group_size, stream) -> int:
 
 def awq_gemm_f16(x, W, bias, y, M, K, N, stream) -> int:
     return load_library().awq_gemm_f16(x, W, bias, y, M, K, N, stream)
+
+
+def awq_dequant_gidx(qweight, qzeros, scales, g_idx, W, K, N, G, stream) -> int:
+    return load_library().awq_dequant_gidx(qweight, qzeros, scales, g_idx, W, K, N, G, stream)
+
+
+def awq_linear_forward_gidx(x, qweight, qzeros, scales, g_idx, bias, y, M, K, N, G, stream) -> int:
+    return load_library().awq_linear_forward_gidx(x, qweight, qzeros, scales, g_idx, bias, y,
+                                                  M, K, N, G, stream)
 
 
 def awq_pack(codes, packed, rows, cols, stream) -> int:

@@ -35,6 +35,8 @@ struct ScratchEntry {
     size_t partial_floats = 0;
     unsigned int *counters = nullptr;
     size_t n_counters = 0;
+    void *w16 = nullptr;           // dequantised weights of the g_idx forward
+    size_t w16_bytes = 0;
 };
 std::map<std::pair<int, cudaStream_t>, ScratchEntry> g_scratch;
 
@@ -95,6 +97,30 @@ bool get_scratch(cudaStream_t stream, size_t partial_floats, size_t n_counters, 
     out->partial_floats = e.partial_floats;
     out->counters = e.counters;
     out->n_counters = e.n_counters;
+    return true;
+}
+
+bool get_w16_scratch(cudaStream_t stream, size_t bytes, void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    ScratchEntry &e = g_scratch[std::make_pair(dev, stream)];
+    if (e.w16_bytes < bytes) {
+        // the old area may still be read by work queued on this stream
+        if (e.w16) {
+            cudaStreamSynchronize(stream);
+            cudaFree(e.w16);
+            e.w16 = nullptr;
+            e.w16_bytes = 0;
+        }
+        if (cudaMalloc(&e.w16, bytes) != cudaSuccess) {
+            e.w16 = nullptr;
+            return false;
+        }
+        e.w16_bytes = bytes;
+    }
+    *out = e.w16;
     return true;
 }
 
@@ -240,6 +266,44 @@ awq_status_t awq_dequant(const int32_t *qweight, const int32_t *qzeros, const vo
     return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
 }
 
+awq_status_t awq_dequant_gidx(const int32_t *qweight, const int32_t *qzeros, const void *scales,
+                              const int32_t *g_idx, void *W, int64_t K, int64_t N, int64_t G,
+                              awq_stream_t stream)
+{
+    if (K <= 0 || N <= 0 || N % 8 != 0 || G <= 0) return AWQ_ERR_INVALID_ARG;
+    if (!qweight || !qzeros || !scales || !g_idx || !W) return AWQ_ERR_INVALID_ARG;
+    if (!aligned16(qweight) || !aligned16(qzeros) || !aligned16(scales) || !aligned16(g_idx) ||
+        !aligned16(W))
+        return AWQ_ERR_MISALIGNED;
+    Problem p{nullptr, qweight, qzeros, scales, nullptr, nullptr, 0, K, N, 0, G};
+    cudaError_t e = awq::launch_dequant_gidx(p, g_idx, W, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+}
+
+awq_status_t awq_linear_forward_gidx(const void *x, const int32_t *qweight, const int32_t *qzeros,
+                                     const void *scales, const int32_t *g_idx, const void *bias,
+                                     void *y, int64_t M, int64_t K, int64_t N, int64_t G,
+                                     awq_stream_t stream)
+{
+    if (M < 0 || K <= 0 || N <= 0 || N % 8 != 0 || G <= 0) return AWQ_ERR_INVALID_ARG;
+    if (!awq::prefill_supported(M > 0 ? M : 1, K, N, 16)) return AWQ_ERR_INVALID_ARG;
+    if (M == 0) return AWQ_OK;
+    if (!x || !qweight || !qzeros || !scales || !g_idx || !y) return AWQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(qweight) || !aligned16(qzeros) || !aligned16(scales) ||
+        !aligned16(g_idx) || !aligned16(y) || (bias && !aligned16(bias)))
+        return AWQ_ERR_MISALIGNED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    void *w16 = nullptr;
+    if (!awq::get_w16_scratch(s, (size_t)K * (size_t)N * 2, &w16)) return AWQ_ERR_CUDA;
+    Problem pw{nullptr, qweight, qzeros, scales, nullptr, nullptr, 0, K, N, 0, G};
+    cudaError_t e = awq::launch_dequant_gidx(pw, g_idx, w16, s);
+    if (e == cudaSuccess) {
+        Problem pg{x, nullptr, nullptr, nullptr, bias, y, M, K, N, K, 1};
+        e = awq::launch_gemm_f16(pg, w16, s);
+    }
+    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+}
+
 awq_status_t awq_pack(const uint8_t *codes, int32_t *packed, int64_t rows, int64_t cols,
                       awq_stream_t stream)
 {
@@ -299,6 +363,7 @@ awq_status_t awq_last_device_status(awq_stream_t stream)
         awq::reset_scratch_counters(dev);
         return AWQ_ERR_TIMEOUT;
     }
+    if (word & awq::kStatusBadIndex) return AWQ_ERR_INVALID_ARG;
     return AWQ_ERR_CUDA;
 }
 
@@ -311,6 +376,7 @@ void awq_shutdown(void)
         cudaSetDevice(kv.first.first);
         if (kv.second.partials) cudaFree(kv.second.partials);
         if (kv.second.counters) cudaFree(kv.second.counters);
+        if (kv.second.w16) cudaFree(kv.second.w16);
     }
     awq::g_scratch.clear();
     cudaSetDevice(prev);

@@ -37,7 +37,54 @@ dequant_kernel(const uint32_t *__restrict__ qweight, const uint32_t *__restrict_
     }
 }
 
+// The same with the group of row k read from g_idx[k]: the "g_idx"
+// (act-order) grouping, G groups of scales and zero points.
+__global__ void __launch_bounds__(256)
+dequant_gidx_kernel(const uint32_t *__restrict__ qweight, const uint32_t *__restrict__ qzeros,
+                    const __half *__restrict__ scales, const int32_t *__restrict__ g_idx,
+                    __half *__restrict__ W, int64_t K, int64_t words, int64_t G,
+                    unsigned int *status)
+{
+    const int64_t total = K * words;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t k = idx / words;
+        const int64_t j = idx - k * words;
+        const int64_t gi = __ldg(g_idx + k);
+        __half w[8];
+        if (gi < 0 || gi >= G) {
+            raise_status(status, kStatusBadIndex);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[i] = __ushort_as_half((unsigned short)0);
+        } else {
+            const uint32_t qw = __ldg(qweight + idx);
+            const uint32_t zw = __ldg(qzeros + gi * words + j);
+            __half s[8];
+            *reinterpret_cast<uint4 *>(s) = __ldg(reinterpret_cast<const uint4 *>(scales + (gi * words + j) * 8));
+            dequant_word(qw, zw, s, w);
+        }
+        *reinterpret_cast<uint4 *>(W + idx * 8) = *reinterpret_cast<const uint4 *>(w);
+    }
+}
+
 } // namespace
+
+cudaError_t launch_dequant_gidx(const Problem &p, const int32_t *g_idx, void *W, cudaStream_t stream)
+{
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t words = p.N / 8;
+    const int64_t total = p.K * words;
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = (int64_t)(sms > 0 ? sms : 1) * 8;
+    if (blocks > cap) blocks = cap;
+    dequant_gidx_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+        reinterpret_cast<const uint32_t *>(p.qweight), reinterpret_cast<const uint32_t *>(p.qzeros),
+        static_cast<const __half *>(p.scales), g_idx, static_cast<__half *>(W), p.K, words, p.G,
+        device_status_word());
+    return cudaGetLastError();
+}
 
 cudaError_t launch_dequant(const Problem &p, void *W, cudaStream_t stream)
 {

@@ -33,14 +33,23 @@ struct Scratch {
 // kStatusTimeout) for kernels to record device-side errors in.
 unsigned int *device_status_word();
 constexpr unsigned int kStatusTimeout = 1u;
+constexpr unsigned int kStatusBadIndex = 2u;   // a group index outside [0, G)
 
 // Scratch for `stream` on the current device, grown to at least the given
 // sizes. Returns false if an allocation failed.
 bool get_scratch(cudaStream_t stream, size_t partial_floats, size_t n_counters, Scratch *out);
 
+// A buffer of at least `bytes` for `stream` on the current device (dequantised
+// weights of the g_idx forward), grown on demand.
+bool get_w16_scratch(cudaStream_t stream, size_t bytes, void **out);
+
 // ---- kernel launchers (each returns the launch's cudaError_t) ----
 
 cudaError_t launch_dequant(const Problem &p, void *W, cudaStream_t stream);
+
+// Dequantisation with the group of row k taken from g_idx[k] (p.G groups);
+// an index outside [0, G) writes zeros for that row and sets kStatusBadIndex.
+cudaError_t launch_dequant_gidx(const Problem &p, const int32_t *g_idx, void *W, cudaStream_t stream);
 
 // Packing of 4-bit codes (uint8, one per byte) into int32 words, and
 // round-to-nearest quantisation of an fp16 W with the problem's scales and

@@ -12,8 +12,8 @@ from __future__ import annotations
 
 import torch
 
-from ._binding import (AWQError, Path, Status, awq_dequant, awq_linear_forward_path, awq_pack,
-                       awq_quantize_rtn)
+from ._binding import (AWQError, Path, Status, awq_dequant, awq_dequant_gidx, awq_linear_forward_gidx,
+                       awq_linear_forward_path, awq_pack, awq_quantize_rtn)
 
 
 def _ptr(t):
@@ -82,6 +82,55 @@ def dequant(qweight: torch.Tensor, qzeros: torch.Tensor, scales: torch.Tensor,
     if st != Status.OK:
         raise AWQError(st, "awq_dequant")
     return out
+
+
+def dequant_gidx(qweight: torch.Tensor, qzeros: torch.Tensor, scales: torch.Tensor,
+                 g_idx: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """W [K, N] fp16 with the group of row k read from g_idx[k] (int32 [K])."""
+    dev = qweight.device
+    if dev.type != "cuda":
+        raise ValueError("the AWQ library runs on CUDA tensors only")
+    _check(qweight, "qweight", torch.int32, dev)
+    _check(qzeros, "qzeros", torch.int32, dev)
+    _check(scales, "scales", torch.float16, dev)
+    _check(g_idx, "g_idx", torch.int32, dev)
+    K, N, G = qweight.shape[0], qweight.shape[1] * 8, scales.shape[0]
+    if out is None:
+        out = torch.empty((K, N), dtype=torch.float16, device=dev)
+    else:
+        _check(out, "out", torch.float16, dev)
+    st = awq_dequant_gidx(_ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(g_idx), _ptr(out), K, N, G,
+                          _stream(dev))
+    if st != Status.OK:
+        raise AWQError(st, "awq_dequant_gidx")
+    return out
+
+
+def linear_forward_gidx(x: torch.Tensor, qweight: torch.Tensor, qzeros: torch.Tensor,
+                        scales: torch.Tensor, g_idx: torch.Tensor, bias: torch.Tensor | None,
+                        out: torch.Tensor | None = None) -> torch.Tensor:
+    """y = x . W + bias with the group of input row k read from g_idx[k]."""
+    dev = qweight.device
+    if dev.type != "cuda":
+        raise ValueError("the AWQ library runs on CUDA tensors only")
+    for t, name, dt in ((x, "x", torch.float16), (qweight, "qweight", torch.int32),
+                        (qzeros, "qzeros", torch.int32), (scales, "scales", torch.float16),
+                        (g_idx, "g_idx", torch.int32)):
+        _check(t, name, dt, dev)
+    if bias is not None:
+        _check(bias, "bias", torch.float16, dev)
+    K, N, G = qweight.shape[0], qweight.shape[1] * 8, scales.shape[0]
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=dev)
+    else:
+        _check(out, "out", torch.float16, dev)
+    st = awq_linear_forward_gidx(_ptr(x2), _ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(g_idx),
+                                 _ptr(bias), _ptr(out), M, K, N, G, _stream(dev))
+    if st != Status.OK:
+        raise AWQError(st, "awq_linear_forward_gidx")
+    return out.reshape(*x.shape[:-1], N)
 
 
 def pack(codes: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:

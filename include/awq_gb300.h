@@ -133,6 +133,34 @@ awq_status_t awq_dequant(const int32_t *qweight, const int32_t *qzeros,
                          int64_t group_size, awq_stream_t stream);
 
 /*
+ * awq_dequant_gidx / awq_linear_forward_gidx -- the "g_idx" grouping variant
+ * (act-order, as in the GPTQ quantisation tuple the Linear Layer Factory page
+ * lists): the group of input row k is read from a table instead of being
+ * k / group_size.
+ *   W[k, n] = fp16_rn((q[k, n] - z[g_idx[k], n]) * scales[g_idx[k], n])
+ *   y[m, n] = fp16_rn(sum_k x[m, k] * W[k, n] + bias[n])
+ *   g_idx   int32 [K], every entry in [0, G)       (read)
+ *   qzeros  int32 [G, N / 8], scales fp16 [G, N]   (read)
+ * Other arguments and layouts as awq_dequant / awq_linear_forward, with the
+ * number of groups G in place of group_size. Requires K > 0, N % 8 == 0,
+ * G > 0 (AWQ_ERR_INVALID_ARG otherwise); the forward also needs K % 16 == 0
+ * and N % 32 == 0. A table entry outside [0, G) cannot be seen before the
+ * kernel runs: that row of W is written as zeros and the next
+ * awq_last_device_status() returns AWQ_ERR_INVALID_ARG.
+ * The forward dequantises W into a per-(device, stream) scratch area of
+ * K x N fp16 (allocated on first use, like the split-K scratch) and runs the
+ * prefill kernel's tcgen05 core on it (as awq_gemm_f16): it reads and writes
+ * W once more than the grouped forward, so it is meant for prefill-sized M.
+ */
+awq_status_t awq_dequant_gidx(const int32_t *qweight, const int32_t *qzeros, const void *scales,
+                              const int32_t *g_idx, void *W, int64_t K, int64_t N, int64_t G,
+                              awq_stream_t stream);
+awq_status_t awq_linear_forward_gidx(const void *x, const int32_t *qweight, const int32_t *qzeros,
+                                     const void *scales, const int32_t *g_idx, const void *bias,
+                                     void *y, int64_t M, int64_t K, int64_t N, int64_t G,
+                                     awq_stream_t stream);
+
+/*
  * awq_pack -- packs 4-bit codes into the layer's int32 format, the inverse of
  * the unpacking every forward call does (I/O Contract of the WQLinear page:
  * eight 4-bit values per int32; the order is this library's reading):
@@ -225,8 +253,9 @@ const char *awq_status_string(awq_status_t status);
  * awq_last_device_status -- synchronises `stream`, then reads and clears the
  * current device's status word. Returns AWQ_OK, AWQ_ERR_TIMEOUT if a kernel's
  * bounded wait ran out since the last read (that kernel wrote no result and
- * the scratch area of the stream it ran on is reset), or AWQ_ERR_CUDA if the
- * synchronisation itself failed.
+ * the scratch area of the stream it ran on is reset), AWQ_ERR_INVALID_ARG if
+ * a g_idx entry was outside [0, G), or AWQ_ERR_CUDA if the synchronisation
+ * itself failed.
  */
 awq_status_t awq_last_device_status(awq_stream_t stream);
 

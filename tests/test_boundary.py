@@ -120,6 +120,27 @@ def test_quantize_null_and_misaligned(lib):
     assert awq.awq_quantize_rtn(A, A, A + 4, B, 256, 64, 128, None) == Status.ERR_MISALIGNED
 
 
+def test_gidx_argument_rules(lib):
+    dq = lambda **k: awq.awq_dequant_gidx(k.get("qw", A), A, A, k.get("gi", A), k.get("W", B),
+                                          k.get("K", 256), k.get("N", 64), k.get("G", 4), None)
+    assert dq(N=12) == Status.ERR_INVALID_ARG
+    assert dq(G=0) == Status.ERR_INVALID_ARG
+    assert dq(K=0) == Status.ERR_INVALID_ARG
+    assert dq(gi=None) == Status.ERR_INVALID_ARG
+    assert dq(gi=A + 4) == Status.ERR_MISALIGNED
+    assert dq(W=B + 2) == Status.ERR_MISALIGNED
+    fw = lambda **k: awq.awq_linear_forward_gidx(k.get("x", A), A, A, A, k.get("gi", A), None, B,
+                                                 k.get("M", 4), k.get("K", 256), k.get("N", 64),
+                                                 k.get("G", 4), None)
+    assert fw(N=40) == Status.ERR_INVALID_ARG      # N % 32 for the tensor-core core
+    assert fw(K=72) == Status.ERR_INVALID_ARG      # K % 16
+    assert fw(G=-1) == Status.ERR_INVALID_ARG
+    assert fw(M=-1) == Status.ERR_INVALID_ARG
+    assert fw(gi=None) == Status.ERR_INVALID_ARG
+    assert fw(x=A + 2) == Status.ERR_MISALIGNED
+    assert fw(M=0) == Status.OK
+
+
 def test_path_support_rules(lib):
     # the generic kernel takes every valid shape, nothing takes an invalid one
     for (M, K, N, g) in [(1, 4096, 8, -1), (3, 48, 104, 16), (5, 336, 800, 48), (1, 1, 8, 1)]:
