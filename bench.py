@@ -268,6 +268,18 @@ def capture_step(items, path, stream, with_events=True):
     return graph, evs
 
 
+def kernels_per_call(M, K, N, g, path_value: int) -> int:
+    """Kernel launches one forward call makes on `path_value`: one, except
+    the dequantise-then-GEMM path, which launches a dequant kernel and a GEMM
+    per window of at most 256 MiB of fp16 weights (256-column multiples),
+    as its documentation in include/awq_gb300.h states."""
+    if path_value != 4:
+        return 1
+    nc = max(256, ((256 << 20) // (2 * K)) // 256 * 256)
+    nc = min(nc, N)
+    return 2 * ((N + nc - 1) // nc)
+
+
 def run_native(args, problems, device):
     import bit_weight_quantized_awq_gb300 as awq
     from bit_weight_quantized_awq_gb300 import Path
@@ -347,7 +359,11 @@ def run_native(args, problems, device):
     return {"elapsed": max_el, "tot_wbytes": tot_wbytes, "tot_flops": tot_flops,
             "wbytes": wbytes, "flops": fl, "abytes": abytes, "clocks": clocks,
             "per_problem": per_problem, "copies": len(sets), "graph_events": use_events,
-            "launches": args.steps * len(problems), "sets": sets}
+            "launches": args.steps * sum(
+                kernels_per_call(p[0], p[1], p[2], p[3],
+                                 int(path) if path != Path.AUTO else awq.awq_select_path(p[0], p[1], p[2], p[3]))
+                for p in problems),
+            "sets": sets}
 
 
 def run_e2e(args, problems, device, sets, steps):
@@ -479,7 +495,7 @@ def run_sweep(args, device, peaks):
     for wl in names:
         for prob in WORKLOADS[wl]:
             M, K, N, g, bias = prob
-            for path in (Path.DECODE, Path.PREFILL, Path.GENERIC):
+            for path in (Path.DECODE, Path.PREFILL, Path.DEQUANT_GEMM, Path.GENERIC):
                 if not awq.awq_path_supported(M, K, N, g, path):
                     continue
                 if path == Path.GENERIC and flops(M, K, N) > 2e11:
@@ -661,7 +677,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="decode-7b", choices=list(WORKLOADS) + ["all", "quantize", "gidx"])
-    ap.add_argument("--path", default="auto", choices=["auto", "generic", "decode", "prefill"])
+    ap.add_argument("--path", default="auto", choices=["auto", "generic", "decode", "prefill", "dequant_gemm"])
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-out", default=None)
     ap.add_argument("--e2e-steps", type=int, default=200)
@@ -702,15 +718,19 @@ def main():
     import bit_weight_quantized_awq_gb300 as awq
     paths = [awq.awq_select_path(p[0], p[1], p[2], p[3]) for p in problems]
     roof, per = None, None
-    names = {1: "generic_forward_kernel", 2: "decode_kernel", 3: "prefill_kernel"}
+    names = {1: "generic_forward_kernel", 2: "decode_kernel", 3: "prefill_kernel",
+             4: "prefill_kernel (GEMM core on dequant_kernel windows)"}
     dominant = max(set(paths), key=paths.count)
-    if all(pth == dominant for pth in paths):
+    # the fused prefill kernel and the dequantise-then-GEMM path both run the
+    # tcgen05 contraction: one tensor-bound family
+    family = lambda pth: 3 if pth in (3, 4) else pth
+    if all(family(pth) == family(dominant) for pth in paths):
         # every launch of the step is the dominant kernel: its average launch
         # duration is the timed region over the launches in it
         launch_s = r["elapsed"] / (args.steps * len(problems))
         achieved = r["abytes"] / len(problems) / launch_s / 1e9
         traffic, traffic_note = ncu_traffic(args.workload)
-        if dominant == 3:
+        if dominant in (3, 4):
             # the tcgen05 contraction: fp16 operands, whose nominal dense rate
             # equals bf16's, so the measured bf16 cuBLAS peak is the roof
             tf = r["flops"] / len(problems) / launch_s / 1e12

@@ -48,6 +48,7 @@ class Path(enum.IntEnum):
     GENERIC = 1
     DECODE = 2
     PREFILL = 3
+    DEQUANT_GEMM = 4
 
 
 class AWQError(RuntimeError):

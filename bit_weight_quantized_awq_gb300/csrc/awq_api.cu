@@ -163,17 +163,28 @@ bool path_fits(const Problem &p, awq_path_t path)
     case AWQ_PATH_GENERIC: return true;
     case AWQ_PATH_DECODE: return awq::decode_supported(p.M, p.K, p.N, p.g);
     case AWQ_PATH_PREFILL: return awq::prefill_supported(p.M, p.K, p.N, p.g);
+    case AWQ_PATH_DEQUANT_GEMM: return awq::prefill_supported(p.M, p.K, p.N, p.g);
     default: return false;
     }
 }
 
 // Largest M served by the decode kernel when both fast paths fit.
 constexpr int64_t kDecodeMaxM = 32;
+// Dequantising the weights once and running the plain tcgen05 GEMM beats
+// dequantising every weight tile once per 128-token tile inside the fused
+// kernel from M = 2048 on (1.15-1.26x at 2048, 1.35-1.44x at 8192 on the
+// 7B/70B shapes), unless K is so long that the extra pass over fp16
+// weights outweighs the saving (K = 28672 at M = 2048: 0.87x): measured
+// rule M >= 2048 and 8 M >= K.
+constexpr int64_t kDequantGemmMinM = 2048;
+
+bool dequant_gemm_pays(const Problem &p) { return p.M >= kDequantGemmMinM && 8 * p.M >= p.K; }
 
 awq_path_t auto_path(const Problem &p)
 {
     if (p.M <= kDecodeMaxM && awq::decode_supported(p.M, p.K, p.N, p.g)) return AWQ_PATH_DECODE;
-    if (awq::prefill_supported(p.M, p.K, p.N, p.g)) return AWQ_PATH_PREFILL;
+    if (awq::prefill_supported(p.M, p.K, p.N, p.g))
+        return dequant_gemm_pays(p) ? AWQ_PATH_DEQUANT_GEMM : AWQ_PATH_PREFILL;
     if (awq::decode_supported(p.M, p.K, p.N, p.g)) return AWQ_PATH_DECODE;
     return AWQ_PATH_GENERIC;
 }
@@ -224,7 +235,7 @@ awq_status_t awq_linear_forward_path(const void *x, const int32_t *qweight, cons
     awq_status_t st = check_shape(K, N, group_size, &g);
     if (st != AWQ_OK) return st;
     if (path != AWQ_PATH_AUTO && path != AWQ_PATH_GENERIC && path != AWQ_PATH_DECODE &&
-        path != AWQ_PATH_PREFILL)
+        path != AWQ_PATH_PREFILL && path != AWQ_PATH_DEQUANT_GEMM)
         return AWQ_ERR_INVALID_ARG;
     if (M == 0) return AWQ_OK;   // empty x and y may be NULL; nothing to do
     if (!x || !qweight || !qzeros || !scales || !y) return AWQ_ERR_INVALID_ARG;
@@ -239,6 +250,7 @@ awq_status_t awq_linear_forward_path(const void *x, const int32_t *qweight, cons
     switch (use) {
     case AWQ_PATH_DECODE: e = awq::launch_decode(p, s); break;
     case AWQ_PATH_PREFILL: e = awq::launch_prefill(p, s); break;
+    case AWQ_PATH_DEQUANT_GEMM: e = awq::launch_dequant_gemm(p, s); break;
     default: e = awq::launch_generic(p, s); break;
     }
     return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;

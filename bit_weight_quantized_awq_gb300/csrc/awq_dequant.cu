@@ -18,15 +18,16 @@ namespace {
 __global__ void __launch_bounds__(256)
 dequant_kernel(const uint32_t *__restrict__ qweight, const uint32_t *__restrict__ qzeros,
                const __half *__restrict__ scales, __half *__restrict__ W,
-               int64_t K, int64_t words, int64_t g)
+               int64_t K, int64_t words, int64_t g, int64_t word0, int64_t wwords)
 {
-    const int64_t total = K * words;
+    // output: words word0 .. word0 + wwords - 1 of every row, as a [K, 8 wwords] array
+    const int64_t total = K * wwords;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t k = idx / words;
-        const int64_t j = idx - k * words;
+        const int64_t k = idx / wwords;
+        const int64_t j = word0 + (idx - k * wwords);
         const int64_t gi = k / g;
-        const uint32_t qw = __ldg(qweight + idx);
+        const uint32_t qw = __ldg(qweight + k * words + j);
         const uint32_t zw = __ldg(qzeros + gi * words + j);
         // 8 scales of columns 8j .. 8j+7: 16 bytes, 16-byte aligned
         const uint4 sraw = __ldg(reinterpret_cast<const uint4 *>(scales + (gi * words + j) * 8));
@@ -86,21 +87,51 @@ cudaError_t launch_dequant_gidx(const Problem &p, const int32_t *g_idx, void *W,
     return cudaGetLastError();
 }
 
-cudaError_t launch_dequant(const Problem &p, void *W, cudaStream_t stream)
+cudaError_t launch_dequant_cols(const Problem &p, int64_t c0, int64_t nc, void *W, cudaStream_t stream)
 {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t words = p.N / 8;
-    const int64_t total = p.K * words;
+    const int64_t total = p.K * (nc / 8);
     const int threads = 256;
     int64_t blocks = (total + threads - 1) / threads;
     const int64_t cap = (int64_t)(sms > 0 ? sms : 1) * 8;
     if (blocks > cap) blocks = cap;
+    if (blocks < 1) return cudaSuccess;
     dequant_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
         reinterpret_cast<const uint32_t *>(p.qweight), reinterpret_cast<const uint32_t *>(p.qzeros),
-        static_cast<const __half *>(p.scales), static_cast<__half *>(W), p.K, words, p.g);
+        static_cast<const __half *>(p.scales), static_cast<__half *>(W), p.K, words, p.g, c0 / 8, nc / 8);
     return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const Problem &p, void *W, cudaStream_t stream)
+{
+    return launch_dequant_cols(p, 0, p.N, W, stream);
+}
+
+// Windows of at most this many bytes of fp16 weights bound the scratch.
+constexpr int64_t kW16WindowBytes = 256ll << 20;
+
+cudaError_t launch_dequant_gemm(const Problem &p, cudaStream_t stream)
+{
+    // window width: a multiple of 256 columns (one GEMM tile), or all of N
+    int64_t nc = (kW16WindowBytes / (2 * p.K)) / 256 * 256;
+    if (nc < 256) nc = 256;
+    if (nc > p.N) nc = p.N;
+    void *w16 = nullptr;
+    if (!get_w16_scratch(stream, (size_t)p.K * (size_t)nc * 2, &w16)) return cudaErrorMemoryAllocation;
+    for (int64_t c0 = 0; c0 < p.N; c0 += nc) {
+        const int64_t w = (p.N - c0 < nc) ? p.N - c0 : nc;
+        cudaError_t e = launch_dequant_cols(p, c0, w, w16, stream);
+        if (e != cudaSuccess) return e;
+        Problem pg{p.x, nullptr, nullptr, nullptr,
+                   p.bias ? static_cast<const __half *>(p.bias) + c0 : nullptr,
+                   static_cast<__half *>(p.y) + c0, p.M, p.K, w, p.K, 1};
+        e = launch_gemm_f16(pg, w16, stream, p.N);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 } // namespace awq

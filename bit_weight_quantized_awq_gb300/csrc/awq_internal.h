@@ -47,6 +47,14 @@ bool get_w16_scratch(cudaStream_t stream, size_t bytes, void **out);
 
 cudaError_t launch_dequant(const Problem &p, void *W, cudaStream_t stream);
 
+// Dequantisation of output columns c0 .. c0 + nc - 1 (multiples of 8) into a
+// [K, nc] fp16 array.
+cudaError_t launch_dequant_cols(const Problem &p, int64_t c0, int64_t nc, void *W, cudaStream_t stream);
+
+// Large-M forward: the weights dequantised once per column window into a
+// per-stream scratch area, then the tcgen05 fp16 GEMM core on each window.
+cudaError_t launch_dequant_gemm(const Problem &p, cudaStream_t stream);
+
 // Dequantisation with the group of row k taken from g_idx[k] (p.G groups);
 // an index outside [0, G) writes zeros for that row and sets kStatusBadIndex.
 cudaError_t launch_dequant_gidx(const Problem &p, const int32_t *g_idx, void *W, cudaStream_t stream);
@@ -70,6 +78,8 @@ cudaError_t launch_prefill(const Problem &p, cudaStream_t stream);
 
 // The prefill kernel's tensor-core pipeline on an already dequantised fp16
 // W [K, N] (no dequant stage): y = x . W + bias. Same shape rules as prefill.
-cudaError_t launch_gemm_f16(const Problem &p, const void *w16, cudaStream_t stream);
+// ldy: elements between rows of y (0 = N), so that a call can write a
+// column window of a wider output.
+cudaError_t launch_gemm_f16(const Problem &p, const void *w16, cudaStream_t stream, int64_t ldy = 0);
 
 } // namespace awq

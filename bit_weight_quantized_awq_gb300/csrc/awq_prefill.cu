@@ -120,6 +120,7 @@ struct PrefillParams {
     float *partials;        // [2 * sk_ctas][kPartialFloats] stream-K partial sums
     unsigned int *arrive;   // [sk_tiles] contributors counted in (zero between calls)
     int M, K, N, g;
+    int64_t ldy;            // elements between rows of y (N, or more for a column window)
     int tiles_m, tiles_n, kiters;
     int dp_waves;           // full waves of whole tiles, tile = cta + wave * gridDim.x
     int sk_tiles;           // tiles after those, split along k between sk_ctas CTAs
@@ -481,7 +482,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 #pragma unroll
                             for (int e = 0; e < 32; ++e) out[e] = __float2half_rn(__uint_as_float(r[e]));
                         }
-                        uint4 *dst = reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.N + col);
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.ldy + col);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) dst[v] = reinterpret_cast<const uint4 *>(out)[v];
                     }
@@ -610,7 +611,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         out[e] = __float2half_rn((kDequant ? acc[j][unperm(e)] : acc[j][e]) + bv[e]);
-                    *reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.N + col) = *reinterpret_cast<const uint4 *>(out);
+                    *reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.ldy + col) = *reinterpret_cast<const uint4 *>(out);
                 }
             }
             // every contributor has counted in: the counter is free for the next call
@@ -691,7 +692,7 @@ LaunchInfo launch_info()
 }
 
 template <bool kDequant, bool kWhole>
-cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream)
+cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int64_t ldy)
 {
     const LaunchInfo li = launch_info<kDequant, kWhole>();
     if (li.err != cudaSuccess) return li.err;
@@ -742,6 +743,7 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream)
     p.y = static_cast<__half *>(pr.y);
     p.status = device_status_word();
     p.M = M; p.K = K; p.N = N; p.g = g;
+    p.ldy = ldy > 0 ? ldy : N;
     p.tiles_m = tiles_m; p.tiles_n = tiles_n; p.kiters = kiters;
     p.dp_waves = dp_waves; p.sk_tiles = sk_tiles; p.sk_ctas = sk_ctas;
     p.stage_tx = tx_bytes;
@@ -768,12 +770,12 @@ cudaError_t launch_prefill(const Problem &p, cudaStream_t stream)
 {
     if (!prefill_supported(p.M, p.K, p.N, p.g)) return cudaErrorInvalidValue;
     // g % 64 == 0: every 64-row stage lies in one group
-    return p.g % BK == 0 ? launch<true, true>(p, nullptr, stream) : launch<true, false>(p, nullptr, stream);
+    return p.g % BK == 0 ? launch<true, true>(p, nullptr, stream, 0) : launch<true, false>(p, nullptr, stream, 0);
 }
 
-cudaError_t launch_gemm_f16(const Problem &p, const void *w16, cudaStream_t stream)
+cudaError_t launch_gemm_f16(const Problem &p, const void *w16, cudaStream_t stream, int64_t ldy)
 {
-    return launch<false, true>(p, w16, stream);
+    return launch<false, true>(p, w16, stream, ldy);
 }
 
 } // namespace awq

@@ -71,7 +71,11 @@ typedef enum {
     AWQ_PATH_AUTO = 0,    /* pick by shape (M against the measured crossover) */
     AWQ_PATH_GENERIC = 1, /* any valid shape; plain CUDA-core kernel */
     AWQ_PATH_DECODE = 2,  /* small M: split-K streaming GEMV-style kernel */
-    AWQ_PATH_PREFILL = 3  /* large M: tcgen05 / TMEM tensor-core kernel */
+    AWQ_PATH_PREFILL = 3, /* large M: tcgen05 / TMEM tensor-core kernel, dequantising in
+                             shared memory */
+    AWQ_PATH_DEQUANT_GEMM = 4 /* very large M: weights dequantised once per window of at
+                             most 256 MB of fp16 into a per-stream scratch area, then the
+                             same kernel's tcgen05 GEMM core on each window */
 } awq_path_t;
 
 /*
@@ -89,6 +93,13 @@ typedef enum {
  *   K, N       in_features, out_features (N % 8 == 0)
  *   group_size g > 0 with K % g == 0, or -1 for g = K
  *   stream     CUDA stream to enqueue on
+ *
+ * Kernel family (AWQ_PATH_AUTO, chosen from measurements on GB300): the
+ * decode kernel for M <= 32; the fused tcgen05 prefill kernel for larger M;
+ * for M >= 2048 with 8 M >= K, the weights dequantised once into a
+ * per-stream scratch area (windows of at most 256 MB of fp16, allocated on
+ * first use) and the same kernel's tcgen05 GEMM core; the generic kernel
+ * for shapes the others do not take.
  *
  * Returns AWQ_ERR_INVALID_ARG for N % 8 != 0, K % g != 0, g == 0, g < -1,
  * M < 0, K <= 0, N <= 0 or a NULL required pointer; AWQ_ERR_MISALIGNED for a

@@ -74,7 +74,7 @@ def run_path(p_gpu: Problem, path: Path, out=None) -> torch.Tensor:
 def paths_for(M: int, K: int, N: int, g: int) -> list[Path]:
     """AUTO plus every explicit path that can serve this shape."""
     out = [Path.AUTO]
-    for path in (Path.GENERIC, Path.DECODE, Path.PREFILL):
+    for path in (Path.GENERIC, Path.DECODE, Path.PREFILL, Path.DEQUANT_GEMM):
         if awq_path_supported(M, K, N, g, path):
             out.append(path)
     return out

@@ -145,14 +145,28 @@ def test_path_support_rules(lib):
     # the generic kernel takes every valid shape, nothing takes an invalid one
     for (M, K, N, g) in [(1, 4096, 8, -1), (3, 48, 104, 16), (5, 336, 800, 48), (1, 1, 8, 1)]:
         assert awq.awq_path_supported(M, K, N, g, Path.GENERIC) == 1
-        assert awq.awq_select_path(M, K, N, g) in (Path.GENERIC, Path.DECODE, Path.PREFILL)
+        assert awq.awq_select_path(M, K, N, g) in (Path.GENERIC, Path.DECODE, Path.PREFILL,
+                                                   Path.DEQUANT_GEMM)
     assert awq.awq_path_supported(1, 4096, 12, 128, Path.GENERIC) == 0
     assert awq.awq_select_path(1, 4096, 12, 128) == -1
     assert awq.awq_select_path(-1, 4096, 4096, 128) == -1
     # a forced path that cannot take the shape is refused before any launch
-    for path in (Path.DECODE, Path.PREFILL):
+    for path in (Path.DECODE, Path.PREFILL, Path.DEQUANT_GEMM):
         if not awq.awq_path_supported(1, 4096, 8, -1, path):
             assert fwd(M=1, K=4096, N=8, g=-1, path=path) == Status.ERR_INVALID_ARG
+
+
+def test_automatic_path_follows_the_measured_crossovers(lib):
+    # decode through 32 tokens, the fused tcgen05 kernel up to 2047, then the
+    # weights dequantised once and the plain tcgen05 GEMM (when 8 M >= K)
+    for M, want in [(1, Path.DECODE), (32, Path.DECODE), (33, Path.PREFILL), (2047, Path.PREFILL),
+                    (2048, Path.DEQUANT_GEMM), (8192, Path.DEQUANT_GEMM)]:
+        assert awq.awq_select_path(M, 4096, 12288, 128) == want, M
+    assert awq.awq_select_path(2048, 28672, 8192, 128) == Path.PREFILL
+    assert awq.awq_select_path(8192, 28672, 8192, 128) == Path.DEQUANT_GEMM
+    for path in (Path.PREFILL, Path.DEQUANT_GEMM):
+        assert awq.awq_path_supported(2048, 4096, 12288, 128, path) == 1
+        assert awq.awq_path_supported(2048, 4100, 12288, -1, path) == 0      # K % 16
 
 
 def test_layer_checks_on_host():
