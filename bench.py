@@ -14,6 +14,7 @@ step, more than twice the 129 MB L2), so each call reads its weights cold.
     python bench.py --sweep --workload all    # per-problem table, every path
     python bench.py --sweep --workload quantize   # awq_quantize_rtn / awq_pack GB/s
     python bench.py --sweep --workload gidx       # awq_linear_forward_gidx TFLOP/s
+    python bench.py --sweep --workload shard      # column/row-sharded layer on one GPU
 
 Timing: one CUDA graph per step (its launches each bracketed by external
 event-record nodes); the timed region replays K steps between a barrier +
@@ -667,6 +668,73 @@ def run_gidx_sweep(args, device, peaks):
         out.close()
 
 
+def run_shard_sweep(args, device, peaks):
+    """Sharded layer on one GPU (the shards one after another): the 70B-class
+    shapes split 2 or 4 ways by columns and by group-aligned rows, against
+    the unsharded forward; weight GB/s or TFLOP/s of the whole sharded
+    forward, CUDA graph of back-to-back forwards over two weight copies."""
+    import bit_weight_quantized_awq_gb300 as awq
+    from bit_weight_quantized_awq_gb300.shard import (column_parallel_forward, row_parallel_forward,
+                                                      split_columns, split_rows)
+    awq.load_library()
+    out = open(args.sweep_out, "w") if args.sweep_out else None
+    stream = torch.cuda.Stream(device)
+    g = 128
+    for (K, N) in SWEEP_SHAPES:
+        for M in (1, 16, 2048):
+            gen = torch.Generator(device=device).manual_seed(0)
+            G = K // g
+            copies = []
+            for _ in range(2):
+                qw = torch.randint(-2**31, 2**31 - 1, (K, N // 8), dtype=torch.int32, device=device, generator=gen)
+                qz = torch.randint(-2**31, 2**31 - 1, (G, N // 8), dtype=torch.int32, device=device, generator=gen)
+                sc = (torch.rand((G, N), device=device, generator=gen) * 9e-3 + 1e-3).half()
+                b = (torch.randn((N,), device=device, generator=gen) * 0.1).half()
+                copies.append((qw, qz, sc, b))
+            x = torch.randn((M, K), device=device, generator=gen).half()
+            for mode, parts in (("unsharded", 1), ("columns", 2), ("columns", 4), ("rows", 2), ("rows", 4)):
+                if mode == "unsharded":
+                    fns = [lambda c=c: awq.linear_forward(x, c[0], c[1], c[2], c[3], g) for c in copies]
+                elif mode == "columns":
+                    sh = [split_columns(c[0], c[1], c[2], c[3], parts) for c in copies]
+                    fns = [lambda s=s: column_parallel_forward(x, s, g) for s in sh]
+                else:
+                    sh = [(split_rows(c[0], c[1], c[2], g, parts), c[3]) for c in copies]
+                    fns = [lambda s=s: row_parallel_forward(x, s[0], s[1]) for s in sh]
+                with torch.cuda.stream(stream):
+                    for f in fns:
+                        f()
+                stream.synchronize()
+                reps = 10
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=stream):
+                    for r in range(reps):
+                        fns[r % 2]()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    graph.replay()
+                    stream.synchronize()
+                    e0.record(stream)
+                    graph.replay()
+                    e1.record(stream)
+                torch.cuda.synchronize(device)
+                t = e0.elapsed_time(e1) / 1e3 / reps
+                row = {"workload": "shard", "mode": mode, "parts": parts, "M": M, "K": K, "N": N,
+                       "us": t * 1e6, "weight_gbs": weight_bytes(K, N, g) / t / 1e9,
+                       "tflops": flops(M, K, N) / t / 1e12,
+                       "hbm_frac": algo_bytes(M, K, N, g, True) / t / 1e9 / peaks["hbm_gbs"],
+                       "tc_frac": flops(M, K, N) / t / 1e12 / peaks["bf16_tflops"]}
+                print(json.dumps(row), file=sys.stderr, flush=True)
+                if out:
+                    out.write(json.dumps(row) + "\n")
+                    out.flush()
+                del graph
+            del copies
+            torch.cuda.empty_cache()
+    if out:
+        out.close()
+
+
 # --------------------------------------------------------------------------
 
 def main():
@@ -676,7 +744,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", default="decode-7b", choices=list(WORKLOADS) + ["all", "quantize", "gidx"])
+    ap.add_argument("--workload", default="decode-7b", choices=list(WORKLOADS) + ["all", "quantize", "gidx", "shard"])
     ap.add_argument("--path", default="auto", choices=["auto", "generic", "decode", "prefill", "dequant_gemm"])
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-out", default=None)
@@ -704,10 +772,12 @@ def main():
             run_quantize_sweep(args, device, peaks)
         elif args.workload == "gidx":
             run_gidx_sweep(args, device, peaks)
+        elif args.workload == "shard":
+            run_shard_sweep(args, device, peaks)
         else:
             run_sweep(args, device, peaks)
         return
-    if args.workload in ("quantize", "gidx"):
+    if args.workload in ("quantize", "gidx", "shard"):
         ap.error(f"--workload {args.workload} is a sweep (--sweep)")
 
     problems = WORKLOADS[args.workload]

@@ -19,7 +19,9 @@ from ._binding import (  # noqa: F401
     awq_last_device_status,
     awq_linear_forward,
     awq_linear_forward_decode_noalloc,
+    awq_finish_rows,
     awq_linear_forward_gidx,
+    awq_linear_forward_rows,
     awq_linear_forward_path,
     awq_pack,
     awq_path_supported,

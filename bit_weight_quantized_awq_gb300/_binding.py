@@ -31,6 +31,8 @@ EXPORTED = (
     "awq_quantize_rtn",
     "awq_dequant_gidx",
     "awq_linear_forward_gidx",
+    "awq_linear_forward_rows",
+    "awq_finish_rows",
 )
 
 
@@ -100,6 +102,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.awq_dequant_gidx.restype = _INT
         lib.awq_linear_forward_gidx.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]
         lib.awq_linear_forward_gidx.restype = _INT
+        lib.awq_linear_forward_rows.argtypes = [_P, _I64, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]
+        lib.awq_linear_forward_rows.restype = _INT
+        lib.awq_finish_rows.argtypes = [_P, _P, _P, _I64, _I64, _P]
+        lib.awq_finish_rows.restype = _INT
         lib.awq_pack.argtypes = [_P, _P, _I64, _I64, _P]
         lib.awq_pack.restype = _INT
         lib.awq_quantize_rtn.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P]
@@ -146,6 +152,15 @@ def awq_dequant_gidx(qweight, qzeros, scales, g_idx, W, K, N, G, stream) -> int:
 def awq_linear_forward_gidx(x, qweight, qzeros, scales, g_idx, bias, y, M, K, N, G, stream) -> int:
     return load_library().awq_linear_forward_gidx(x, qweight, qzeros, scales, g_idx, bias, y,
                                                   M, K, N, G, stream)
+
+
+def awq_linear_forward_rows(x, ldx, qweight, qzeros, scales, y32, M, K, N, group_size, stream) -> int:
+    return load_library().awq_linear_forward_rows(x, ldx, qweight, qzeros, scales, y32, M, K, N,
+                                                  group_size, stream)
+
+
+def awq_finish_rows(y32, bias, y, M, N, stream) -> int:
+    return load_library().awq_finish_rows(y32, bias, y, M, N, stream)
 
 
 def awq_pack(codes, packed, rows, cols, stream) -> int:

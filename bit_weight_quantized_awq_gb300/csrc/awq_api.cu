@@ -278,6 +278,46 @@ awq_status_t awq_dequant(const int32_t *qweight, const int32_t *qzeros, const vo
     return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
 }
 
+awq_status_t awq_linear_forward_rows(const void *x, int64_t ldx, const int32_t *qweight,
+                                     const int32_t *qzeros, const void *scales, float *y32,
+                                     int64_t M, int64_t K, int64_t N, int64_t group_size,
+                                     awq_stream_t stream)
+{
+    int64_t g = 0;
+    if (M < 0) return AWQ_ERR_INVALID_ARG;
+    awq_status_t st = check_shape(K, N, group_size, &g);
+    if (st != AWQ_OK) return st;
+    if (ldx < K || ldx % 8 != 0) return AWQ_ERR_INVALID_ARG;
+    if (M == 0) return AWQ_OK;
+    if (!x || !qweight || !qzeros || !scales || !y32) return AWQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(qweight) || !aligned16(qzeros) || !aligned16(scales) ||
+        !aligned16(y32))
+        return AWQ_ERR_MISALIGNED;
+    Problem p{x, qweight, qzeros, scales, nullptr, nullptr, M, K, N, g, K / g};
+    p.ldx = ldx;
+    p.y32 = y32;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (auto_path(p)) {
+    case AWQ_PATH_DECODE: e = awq::launch_decode(p, s); break;
+    case AWQ_PATH_PREFILL: e = awq::launch_prefill(p, s); break;
+    case AWQ_PATH_DEQUANT_GEMM: e = awq::launch_dequant_gemm(p, s); break;
+    default: e = awq::launch_generic(p, s); break;
+    }
+    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+}
+
+awq_status_t awq_finish_rows(const float *y32, const void *bias, void *y, int64_t M, int64_t N,
+                             awq_stream_t stream)
+{
+    if (M < 0 || N <= 0 || N % 8 != 0) return AWQ_ERR_INVALID_ARG;
+    if (M == 0) return AWQ_OK;
+    if (!y32 || !y) return AWQ_ERR_INVALID_ARG;
+    if (!aligned16(y32) || !aligned16(y) || (bias && !aligned16(bias))) return AWQ_ERR_MISALIGNED;
+    cudaError_t e = awq::launch_finish_rows(y32, bias, y, M, N, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+}
+
 awq_status_t awq_dequant_gidx(const int32_t *qweight, const int32_t *qzeros, const void *scales,
                               const int32_t *g_idx, void *W, int64_t K, int64_t N, int64_t G,
                               awq_stream_t stream)

@@ -101,6 +101,7 @@ static_assert(16 * (kMaxTokens / 8) * Geo<1>::kColWarps * 32 * 4 <= kWBytes, "fo
 struct DecodeParams {
     const __half *bias;
     __half *y;
+    float *y32;             // if set: y32 += the fp32 sums (no bias, no rounding) instead of y
     float *partials;        // [2 * ctas][8 MT][tile columns]
     unsigned int *arrive;   // [tiles]
     unsigned int *status;
@@ -487,6 +488,17 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                         for (int e = 0; e < 2; ++e) {
                             const int m = 8 * mt + 2 * tq + e;
                             if (m < p.M && col0 < p.N) {
+                                if (p.y32) {
+                                    float4 *d = reinterpret_cast<float4 *>(p.y32 + (int64_t)m * p.N + col0);
+                                    float4 lo = d[0], hi = d[1];
+                                    lo.x += acc[0][mt][e]; lo.y += acc[0][mt][2 + e];
+                                    lo.z += acc[1][mt][e]; lo.w += acc[1][mt][2 + e];
+                                    hi.x += acc[2][mt][e]; hi.y += acc[2][mt][2 + e];
+                                    hi.z += acc[3][mt][e]; hi.w += acc[3][mt][2 + e];
+                                    d[0] = lo;
+                                    d[1] = hi;
+                                    continue;
+                                }
                                 __align__(16) __half out[8];
 #pragma unroll
                                 for (int b = 0; b < 4; ++b) {
@@ -605,6 +617,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         const int m = pos / (kTileCols / 4);
         const int col = t * kTileCols + (pos % (kTileCols / 4)) * 4;
         if (col >= p.N) continue;
+        if (p.y32) {
+            float4 *d = reinterpret_cast<float4 *>(p.y32 + (int64_t)m * p.N + col);
+            float4 v = *d;
+            v.x += acc4[k].x; v.y += acc4[k].y; v.z += acc4[k].z; v.w += acc4[k].w;
+            *d = v;
+            continue;
+        }
         float b[4] = {0.f, 0.f, 0.f, 0.f};
         if (p.bias) {
             const uint2 braw = *reinterpret_cast<const uint2 *>(p.bias + col);
@@ -678,7 +697,8 @@ bool build_maps(const Problem &pr, int mpad, CUtensorMap *tw, CUtensorMap *tx, C
     const uint64_t K = (uint64_t)pr.K, N = (uint64_t)pr.N, M = (uint64_t)pr.M, Gn = (uint64_t)pr.G;
     const int R = group_rows_per_stage(pr.g, G::kStageRows);
     // x viewed as [M][K / 64][64]: one box covers a stage's k for every token
-    const uint64_t xd[3] = {64, K / 64, M}, xs[2] = {128, K * 2};
+    const uint64_t ldx = pr.ldx > 0 ? (uint64_t)pr.ldx : K;
+    const uint64_t xd[3] = {64, K / 64, M}, xs[2] = {128, ldx * 2};
     const uint32_t xb[3] = {64, (uint32_t)G::kKBlocks, (uint32_t)mpad};
     bool ok = make_map(tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.x, 3, xd, xs, xb, CU_TENSOR_MAP_SWIZZLE_128B);
     if (CW == 1) {
@@ -765,6 +785,7 @@ cudaError_t prepare(const Problem &pr, int max_ctas, CUtensorMap *maps, DecodePa
         return cudaErrorInvalidValue;
     p->bias = static_cast<const __half *>(pr.bias);
     p->y = static_cast<__half *>(pr.y);
+    p->y32 = pr.y32;
     p->status = device_status_word();
     p->M = (int)pr.M; p->K = (int)pr.K; p->N = (int)pr.N; p->g = (int)pr.g;
     p->tiles = tiles; p->kiters = kiters; p->total = (int)total; p->ctas = ctas;

@@ -127,11 +127,49 @@ cudaError_t launch_dequant_gemm(const Problem &p, cudaStream_t stream)
         if (e != cudaSuccess) return e;
         Problem pg{p.x, nullptr, nullptr, nullptr,
                    p.bias ? static_cast<const __half *>(p.bias) + c0 : nullptr,
-                   static_cast<__half *>(p.y) + c0, p.M, p.K, w, p.K, 1};
+                   p.y ? static_cast<__half *>(p.y) + c0 : nullptr, p.M, p.K, w, p.K, 1};
+        pg.ldx = p.ldx;
+        pg.y32 = p.y32 ? p.y32 + c0 : nullptr;
         e = launch_gemm_f16(pg, w16, stream, p.N);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+__global__ void __launch_bounds__(256)
+finish_rows_kernel(const float4 *__restrict__ y32, const __half *__restrict__ bias,
+                   uint2 *__restrict__ y, int64_t quads, int64_t n_quads)
+{
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < quads;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const float4 v = __ldg(y32 + i);
+        float b[4] = {0.f, 0.f, 0.f, 0.f};
+        if (bias) {
+            const int64_t c = (i % n_quads) * 4;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) b[e] = __half2float(bias[c + e]);
+        }
+        __align__(8) __half out[4] = {__float2half_rn(v.x + b[0]), __float2half_rn(v.y + b[1]),
+                                      __float2half_rn(v.z + b[2]), __float2half_rn(v.w + b[3])};
+        y[i] = *reinterpret_cast<const uint2 *>(out);
+    }
+}
+
+cudaError_t launch_finish_rows(const float *y32, const void *bias, void *y, int64_t M, int64_t N,
+                               cudaStream_t stream)
+{
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t quads = M * N / 4;
+    int64_t blocks = (quads + 255) / 256;
+    const int64_t cap = (int64_t)(sms > 0 ? sms : 1) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) return cudaSuccess;
+    finish_rows_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+        reinterpret_cast<const float4 *>(y32), static_cast<const __half *>(bias), static_cast<uint2 *>(y),
+        quads, N / 4);
+    return cudaGetLastError();
 }
 
 } // namespace awq

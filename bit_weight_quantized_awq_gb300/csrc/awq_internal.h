@@ -18,6 +18,9 @@ struct Problem {
     const void *bias;       // fp16 [N] or nullptr
     void *y;                // fp16 [M, N]
     int64_t M, K, N, g, G;
+    int64_t ldx = 0;        // elements between rows of x (0 = K): a K-slice of a wider x
+    float *y32 = nullptr;   // if set: y32[M, N] += x . W in fp32 (no bias, no rounding),
+                            // instead of writing y
 };
 
 // Per-(device, stream) scratch: fp32 split-K partials plus self-resetting
@@ -58,6 +61,10 @@ cudaError_t launch_dequant_gemm(const Problem &p, cudaStream_t stream);
 // Dequantisation with the group of row k taken from g_idx[k] (p.G groups);
 // an index outside [0, G) writes zeros for that row and sets kStatusBadIndex.
 cudaError_t launch_dequant_gidx(const Problem &p, const int32_t *g_idx, void *W, cudaStream_t stream);
+
+// y[M, N] = fp16_rn(y32 + bias): the end of a row-parallel forward.
+cudaError_t launch_finish_rows(const float *y32, const void *bias, void *y, int64_t M, int64_t N,
+                               cudaStream_t stream);
 
 // Packing of 4-bit codes (uint8, one per byte) into int32 words, and
 // round-to-nearest quantisation of an fp16 W with the problem's scales and

@@ -116,6 +116,7 @@ constexpr uint32_t kIdesc = tc::idesc_f16_f32(BM, BN, true);
 struct PrefillParams {
     const __half *bias;
     __half *y;
+    float *y32;             // if set: y32 += the fp32 sums (no bias, no rounding) instead of y
     unsigned int *status;
     float *partials;        // [2 * sk_ctas][kPartialFloats] stream-K partial sums
     unsigned int *arrive;   // [sk_tiles] contributors counted in (zero between calls)
@@ -468,7 +469,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 #pragma unroll
                     for (int e = 0; e < 32; ++e) r[e] = kDequant ? raw[(e & ~7) + unperm(e & 7)] : raw[e];
                     const int col = n0 + 32 * c;
-                    if (col < p.N && m < p.M) {
+                    if (col < p.N && m < p.M && p.y32) {
+                        float4 *d = reinterpret_cast<float4 *>(p.y32 + (int64_t)m * p.ldy + col);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            float4 t = d[v];
+                            t.x += __uint_as_float(r[4 * v]);
+                            t.y += __uint_as_float(r[4 * v + 1]);
+                            t.z += __uint_as_float(r[4 * v + 2]);
+                            t.w += __uint_as_float(r[4 * v + 3]);
+                            d[v] = t;
+                        }
+                    } else if (col < p.N && m < p.M) {
                         __align__(16) __half out[32];
                         if (p.bias) {
                             __align__(16) __half bh[32];
@@ -598,6 +610,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     const int m = m0 + row;
                     const int col = n0 + (c0 + cc) * 32 + grp * 8;
                     if (m >= p.M || col >= p.N) continue;
+                    if (p.y32) {
+                        float4 *d = reinterpret_cast<float4 *>(p.y32 + (int64_t)m * p.ldy + col);
+                        float4 lo = d[0], hi = d[1];
+                        const float *a8 = acc[j];
+                        float o[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[e] = kDequant ? a8[unperm(e)] : a8[e];
+                        lo.x += o[0]; lo.y += o[1]; lo.z += o[2]; lo.w += o[3];
+                        hi.x += o[4]; hi.y += o[5]; hi.z += o[6]; hi.w += o[7];
+                        d[0] = lo;
+                        d[1] = hi;
+                        continue;
+                    }
                     float bv[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) bv[e] = 0.f;
@@ -716,7 +741,8 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int6
     if (sk_units >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
 
     CUtensorMap tx, tw, ts, tz;
-    bool ok = make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.x, K, M, (uint64_t)K * 2, BK, BM,
+    const uint64_t ldx = pr.ldx > 0 ? (uint64_t)pr.ldx : (uint64_t)K;
+    bool ok = make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.x, K, M, ldx * 2, BK, BM,
                           CU_TENSOR_MAP_SWIZZLE_128B);
     uint32_t tx_bytes = kABytes;
     if (kDequant) {
@@ -741,6 +767,7 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int6
     PrefillParams p{};
     p.bias = static_cast<const __half *>(pr.bias);
     p.y = static_cast<__half *>(pr.y);
+    p.y32 = pr.y32;
     p.status = device_status_word();
     p.M = M; p.K = K; p.N = N; p.g = g;
     p.ldy = ldy > 0 ? ldy : N;

@@ -144,6 +144,31 @@ awq_status_t awq_dequant(const int32_t *qweight, const int32_t *qzeros,
                          int64_t group_size, awq_stream_t stream);
 
 /*
+ * awq_linear_forward_rows / awq_finish_rows -- one piece of a row-parallel
+ * (K-sharded) WQLinear and its end (the Tensor Parallel Layers page's
+ * RowLinear: every shard holds a group-aligned slice of in_features, and the
+ * partial results are summed before the bias is added).
+ *   awq_linear_forward_rows: y32[M, N] += x[:, 0:K] . W[K, N] in fp32 -- no
+ *     bias, no rounding -- where x has row pitch ldx >= K (a K-slice of a
+ *     wider x: pass x + k0 and the full width), W is this shard's qweight /
+ *     qzeros / scales (K rows, group_size as awq_linear_forward), y32 fp32
+ *     [M, N] is caller-allocated and read and written. ldx % 8 == 0. The
+ *     kernel family is chosen as for awq_linear_forward.
+ *   awq_finish_rows: y[M, N] = fp16_rn(y32 + bias[N]) (bias may be NULL).
+ * On one GPU, zeroing y32, calling awq_linear_forward_rows once per shard
+ * on the same stream and then awq_finish_rows gives the unsharded forward
+ * up to the order of the fp32 sums; across GPUs the y32 of all shards would
+ * be summed (an all-reduce) before awq_finish_rows. Argument errors as
+ * awq_linear_forward (AWQ_ERR_INVALID_ARG also for ldx < K or ldx % 8 != 0).
+ */
+awq_status_t awq_linear_forward_rows(const void *x, int64_t ldx, const int32_t *qweight,
+                                     const int32_t *qzeros, const void *scales, float *y32,
+                                     int64_t M, int64_t K, int64_t N, int64_t group_size,
+                                     awq_stream_t stream);
+awq_status_t awq_finish_rows(const float *y32, const void *bias, void *y, int64_t M, int64_t N,
+                             awq_stream_t stream);
+
+/*
  * awq_dequant_gidx / awq_linear_forward_gidx -- the "g_idx" grouping variant
  * (act-order, as in the GPTQ quantisation tuple the Linear Layer Factory page
  * lists): the group of input row k is read from a table instead of being

@@ -141,6 +141,24 @@ def test_gidx_argument_rules(lib):
     assert fw(M=0) == Status.OK
 
 
+def test_row_piece_argument_rules(lib):
+    rows = lambda **k: awq.awq_linear_forward_rows(k.get("x", A), k.get("ldx", 256), A, A, A, k.get("y32", B),
+                                                   k.get("M", 4), k.get("K", 256), k.get("N", 64),
+                                                   k.get("g", 128), None)
+    assert rows(ldx=128) == Status.ERR_INVALID_ARG     # ldx < K
+    assert rows(ldx=260) == Status.ERR_INVALID_ARG     # ldx % 8
+    assert rows(N=12) == Status.ERR_INVALID_ARG
+    assert rows(M=-1) == Status.ERR_INVALID_ARG
+    assert rows(y32=None) == Status.ERR_INVALID_ARG
+    assert rows(x=A + 2) == Status.ERR_MISALIGNED
+    assert rows(y32=B + 4) == Status.ERR_MISALIGNED
+    assert rows(M=0, x=None, y32=None) == Status.OK
+    assert awq.awq_finish_rows(A, None, B, 4, 12, None) == Status.ERR_INVALID_ARG
+    assert awq.awq_finish_rows(None, None, B, 4, 64, None) == Status.ERR_INVALID_ARG
+    assert awq.awq_finish_rows(A, A + 2, B, 4, 64, None) == Status.ERR_MISALIGNED
+    assert awq.awq_finish_rows(None, None, None, 0, 64, None) == Status.OK
+
+
 def test_path_support_rules(lib):
     # the generic kernel takes every valid shape, nothing takes an invalid one
     for (M, K, N, g) in [(1, 4096, 8, -1), (3, 48, 104, 16), (5, 336, 800, 48), (1, 1, 8, 1)]:
