@@ -48,14 +48,30 @@ METRIC = "AWQ W4A16 GEMM TFLOP/s and weight GB/s vs M (1..8192), % of roofline, 
 # launches), valid only while the kernel sources hash to what was captured.
 NCU_TRAFFIC = {
     "decode-7b": {
-        "bytes_per_launch": 26411115,
+        "bytes_per_launch": 26414571,
         "sources": {
             "bit_weight_quantized_awq_gb300/csrc/awq_decode.cu":
-                "d527ef2771be7e23a335bbe4e89eb8a9861b6d2a53532fc6b3350ffe65fd37ee",
+                "e4079f348ce343b8b09f5e0ccba713ff09de901ebcbeeceacaf35185bc6ad29b",
             "bit_weight_quantized_awq_gb300/csrc/awq_device.cuh":
                 "3b7d583fc00ea3a961fa897260e5f0245bcdd8b06cb38725fdece027d0787054",
         },
         "summary": "profiles/decode_kernel_decode-7b.md",
+    },
+    # per forward call: the step's 15 launches (3 fused prefill, 6 dequant +
+    # 6 GEMM) over its 9 calls
+    "prefill-7b": {
+        "bytes_per_launch": 738613889,
+        "sources": {
+            "bit_weight_quantized_awq_gb300/csrc/awq_prefill.cu":
+                "98399862eabd04a14d05a650de9a5dd60cf78e569b6864672dfa9b1b3f44370d",
+            "bit_weight_quantized_awq_gb300/csrc/awq_tcgen05.cuh":
+                "7583bdc482c3f999df48aafe74db217e2c2055ec6f41779622d85db462730d4a",
+            "bit_weight_quantized_awq_gb300/csrc/awq_dequant.cu":
+                "cec5728e91e39c90e73d8a6e73afe2801cc54080a93caa8cb51a8776aec127d4",
+            "bit_weight_quantized_awq_gb300/csrc/awq_device.cuh":
+                "3b7d583fc00ea3a961fa897260e5f0245bcdd8b06cb38725fdece027d0787054",
+        },
+        "summary": "profiles/prefill_kernel_prefill-7b.md",
     },
 }
 
@@ -270,15 +286,14 @@ def capture_step(items, path, stream, with_events=True):
 
 
 def kernels_per_call(M, K, N, g, path_value: int) -> int:
-    """Kernel launches one forward call makes on `path_value`: one, except
-    the dequantise-then-GEMM path, which launches a dequant kernel and a GEMM
-    per window of at most 256 MiB of fp16 weights (256-column multiples),
-    as its documentation in include/awq_gb300.h states."""
-    if path_value != 4:
-        return 1
-    nc = max(256, ((256 << 20) // (2 * K)) // 256 * 256)
-    nc = min(nc, N)
-    return 2 * ((N + nc - 1) // nc)
+    """Kernel launches one forward call makes on `path_value`, as the library
+    plans them (awq_forward_launches: the persistent kernel, the stream-K sum
+    kernel when a tile is split, dequant windows)."""
+    import bit_weight_quantized_awq_gb300 as awq
+    n = awq.awq_forward_launches(M, K, N, g, path_value)
+    if n < 0:
+        raise RuntimeError(f"no launch plan for M={M} K={K} N={N} g={g} path={path_value}")
+    return n
 
 
 def run_native(args, problems, device):

@@ -27,6 +27,7 @@ from ._binding import (  # noqa: F401
     awq_path_supported,
     awq_quantize_rtn,
     awq_select_path,
+    awq_forward_launches,
     awq_shutdown,
     awq_status_string,
     load_library,

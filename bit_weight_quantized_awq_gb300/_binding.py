@@ -21,6 +21,7 @@ EXPORTED = (
     "awq_linear_forward_path",
     "awq_path_supported",
     "awq_select_path",
+    "awq_forward_launches",
     "awq_dequant",
     "awq_status_string",
     "awq_last_device_status",
@@ -88,6 +89,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.awq_path_supported.restype = _INT
         lib.awq_select_path.argtypes = [_I64, _I64, _I64, _I64]
         lib.awq_select_path.restype = _INT
+        lib.awq_forward_launches.argtypes = [_I64, _I64, _I64, _I64, _INT]
+        lib.awq_forward_launches.restype = _INT
         lib.awq_dequant.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P]
         lib.awq_dequant.restype = _INT
         lib.awq_status_string.argtypes = [_INT]
@@ -135,6 +138,10 @@ def awq_path_supported(M, K, N, group_size, path) -> int:
 
 def awq_select_path(M, K, N, group_size) -> int:
     return load_library().awq_select_path(M, K, N, group_size)
+
+
+def awq_forward_launches(M, K, N, group_size, path=0) -> int:
+    return load_library().awq_forward_launches(M, K, N, group_size, int(path))
 
 
 def awq_dequant(qweight, qzeros, scales, W, K, N, group_size, stream) -> int:

@@ -225,6 +225,29 @@ int awq_select_path(int64_t M, int64_t K, int64_t N, int64_t group_size)
     return (int)auto_path(p);
 }
 
+int awq_forward_launches(int64_t M, int64_t K, int64_t N, int64_t group_size, awq_path_t path)
+{
+    int64_t g = 0;
+    if (M < 0 || check_shape(K, N, group_size, &g) != AWQ_OK) return -1;
+    if (M == 0) return 0;
+    Problem p{};
+    p.M = M; p.K = K; p.N = N; p.g = g; p.G = K / g;
+    if (path == AWQ_PATH_AUTO) path = auto_path(p);
+    else if (!path_fits(p, path)) return -1;
+    if (path == AWQ_PATH_DECODE || path == AWQ_PATH_GENERIC) return 1;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return -1;
+    if (path == AWQ_PATH_PREFILL) return awq::prefill_launches(M, K, N, sms);
+    // AWQ_PATH_DEQUANT_GEMM: per window, the dequant kernel and the GEMM core
+    const int64_t nc = awq::dequant_gemm_window(K, N);
+    int n = 0;
+    for (int64_t c0 = 0; c0 < N; c0 += nc)
+        n += 1 + awq::prefill_launches(M, K, N - c0 < nc ? N - c0 : nc, sms);
+    return n;
+}
+
 awq_status_t awq_linear_forward_path(const void *x, const int32_t *qweight, const int32_t *qzeros,
                                      const void *scales, const void *bias, void *y, int64_t M,
                                      int64_t K, int64_t N, int64_t group_size, awq_stream_t stream,

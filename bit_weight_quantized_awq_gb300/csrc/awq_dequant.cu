@@ -113,12 +113,18 @@ cudaError_t launch_dequant(const Problem &p, void *W, cudaStream_t stream)
 // Windows of at most this many bytes of fp16 weights bound the scratch.
 constexpr int64_t kW16WindowBytes = 256ll << 20;
 
-cudaError_t launch_dequant_gemm(const Problem &p, cudaStream_t stream)
+int64_t dequant_gemm_window(int64_t K, int64_t N)
 {
     // window width: a multiple of 256 columns (one GEMM tile), or all of N
-    int64_t nc = (kW16WindowBytes / (2 * p.K)) / 256 * 256;
+    int64_t nc = (kW16WindowBytes / (2 * K)) / 256 * 256;
     if (nc < 256) nc = 256;
-    if (nc > p.N) nc = p.N;
+    if (nc > N) nc = N;
+    return nc;
+}
+
+cudaError_t launch_dequant_gemm(const Problem &p, cudaStream_t stream)
+{
+    const int64_t nc = dequant_gemm_window(p.K, p.N);
     void *w16 = nullptr;
     if (!get_w16_scratch(stream, (size_t)p.K * (size_t)nc * 2, &w16)) return cudaErrorMemoryAllocation;
     for (int64_t c0 = 0; c0 < p.N; c0 += nc) {

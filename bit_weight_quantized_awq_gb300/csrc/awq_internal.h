@@ -88,5 +88,10 @@ cudaError_t launch_prefill(const Problem &p, cudaStream_t stream);
 // ldy: elements between rows of y (0 = N), so that a call can write a
 // column window of a wider output.
 cudaError_t launch_gemm_f16(const Problem &p, const void *w16, cudaStream_t stream, int64_t ldy = 0);
+// kernels one prefill / GEMM-core launch enqueues on a GPU with `sms` SMs:
+// the persistent kernel, plus sk_fixup_kernel when a tile is split along k
+int prefill_launches(int64_t M, int64_t K, int64_t N, int sms);
+// fp16 weight columns per window of the dequantise-then-GEMM path
+int64_t dequant_gemm_window(int64_t K, int64_t N);
 
 } // namespace awq

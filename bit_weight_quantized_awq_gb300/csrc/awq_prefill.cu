@@ -119,7 +119,6 @@ struct PrefillParams {
     float *y32;             // if set: y32 += the fp32 sums (no bias, no rounding) instead of y
     unsigned int *status;
     float *partials;        // [2 * sk_ctas][kPartialFloats] stream-K partial sums
-    unsigned int *arrive;   // [sk_tiles] contributors counted in (zero between calls)
     int M, K, N, g;
     int64_t ldy;            // elements between rows of y (N, or more for a column window)
     int tiles_m, tiles_n, kiters;
@@ -240,12 +239,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     uint64_t *drain = acc_empty + 2;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    volatile int *fix_count = abort_flag + 1;        // stream-K tiles this CTA finishes
-    volatile int *fix_tiles = abort_flag + 2;        // [2]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const Segments sg(p);
+    // the stream-K finishing kernel (or the next layer's kernel) may be
+    // scheduled now; it waits for this grid to complete before reading
+    ptx::launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -262,7 +262,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         }
         ptx::mbar_init(ptx::smem_addr(drain), 1);
         *abort_flag = 0;
-        *fix_count = 0;
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -440,8 +439,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                 // TMEM lane quarter this warp may read
-        const int et = threadIdx.x - kEpilogueWarp0 * 32;   // 0..127
-        const int sk_units = p.sk_tiles * p.kiters;
         int acc_it = 0;
         for (int si = 0; si < sg.count; ++si, ++acc_it) {
             int tile, kb0, kb1;
@@ -504,11 +501,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 continue;
             }
             // ---- a piece of a stream-K tile: store the fp32 partial (first
-            //      piece of this CTA's range in slot 0, last in slot 1), free
-            //      the accumulator and count in. The contributor that counts
-            //      in last finishes the tile after its own loop (below), with
-            //      every warp of the CTA; nobody waits for anybody.
-            const int t = tile - p.dp_waves * (int)gridDim.x;   // stream-K tile index
+            //      piece of this CTA's range in slot 0, last in slot 1) and
+            //      free the accumulator; sk_fixup_kernel, launched after this
+            //      grid, sums the pieces of every split tile.
             float *mine = p.partials + (int64_t)(2 * (int)blockIdx.x + (si == sg.dp ? 0 : 1)) * kPartialFloats;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
@@ -524,123 +519,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             }
             tc::fence_before_sync();
             ptx::mbar_arrive(ptx::smem_addr(acc_empty + abuf));
-            __threadfence();
-            ptx::named_barrier(1, kEpilogueThreads);
-            if (et == 0) {
-                const int cf = sk_cta_of(t * p.kiters, sk_units, p.sk_ctas);
-                const int cl = sk_cta_of(t * p.kiters + p.kiters - 1, sk_units, p.sk_ctas);
-                const unsigned int before = atomicAdd(p.arrive + t, 1u);
-                if (before == (unsigned int)(cl - cf)) fix_tiles[(*fix_count)++] = t;
-            }
-        }
-    }
-    __syncthreads();
-
-    // ---- finish the stream-K tiles this CTA counted in last for (at most
-    //      two). Every role is done, so the stage ring and the B slots are
-    //      free: the partials of all contributors are brought in with
-    //      asynchronous 16-byte copies (many in flight per thread), summed
-    //      in contributor order, the bias added, rounded once and stored.
-    //      Nothing writes the flags read here after the barrier above.
-    if (*fix_count > 0 && !*abort_flag) {
-        __threadfence();
-        const int sk_units = p.sk_tiles * p.kiters;
-        constexpr int kChunkFloats = BM * 32;              // one 32-column chunk of a partial
-        constexpr int kChunkBytes = kChunkFloats * 4;      // 16 KB
-        constexpr int kFixBytes = C::kBarOff;              // ring + B slots
-        constexpr int kUnitsPerThread = (3 * BM * 4 + kThreads - 1) / kThreads;   // <= 3 chunks a round
-        const uint32_t stage_base = ptx::smem_addr(smem);
-        for (int f = 0; f < *fix_count; ++f) {
-            const int t = fix_tiles[f];
-            const int tile = p.dp_waves * (int)gridDim.x + t;
-            const int m0 = (tile % p.tiles_m) * BM;
-            const int n0 = (tile / p.tiles_m) * BN;
-            const int cf = sk_cta_of(t * p.kiters, sk_units, p.sk_ctas);
-            const int n = sk_cta_of(t * p.kiters + p.kiters - 1, sk_units, p.sk_ctas) - cf + 1;
-            // chunks per round and contributors per batch that fit the free space
-            const int nc = std::max(1, std::min(3, kFixBytes / (n * kChunkBytes)));
-            const int batch = kFixBytes / (nc * kChunkBytes);
-            for (int c0 = 0; c0 < BN / 32; c0 += nc) {
-                const int ncr = std::min(nc, BN / 32 - c0);
-                const int units = ncr * BM * 4;            // (chunk, row, 8-column group)
-                float acc[kUnitsPerThread][8];
-#pragma unroll
-                for (int j = 0; j < kUnitsPerThread; ++j)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
-                for (int b0 = 0; b0 < n; b0 += batch) {
-                    const int nb = std::min(batch, n - b0);
-                    // chunks c0 .. c0 + ncr - 1 of a partial are one contiguous block
-                    const int pieces = ncr * (kChunkBytes / 16);
-                    for (int i = 0; i < nb; ++i) {
-                        const int ci = cf + b0 + i;
-                        const int which = (sk_range_begin(ci, sk_units, p.sk_ctas) / p.kiters == t) ? 0 : 1;
-                        const float *src = p.partials + (int64_t)(2 * ci + which) * kPartialFloats +
-                                           (int64_t)c0 * kChunkFloats;
-                        const uint32_t dst = stage_base + (uint32_t)(i * pieces) * 16;
-                        for (int pc = threadIdx.x; pc < pieces; pc += kThreads)
-                            ptx::cp_async_16(dst + (uint32_t)pc * 16, src + pc * 4);
-                    }
-                    ptx::cp_async_wait_all();
-                    __syncthreads();
-#pragma unroll
-                    for (int j = 0; j < kUnitsPerThread; ++j) {
-                        const int u = threadIdx.x + j * kThreads;
-                        if (u >= units) continue;
-                        const int cc = u / (BM * 4);
-                        const int row = u % BM;
-                        const int grp = (u / BM) % 4;
-                        for (int i = 0; i < nb; ++i) {
-                            const float4 *blk = reinterpret_cast<const float4 *>(smem + (size_t)(i * ncr + cc) * kChunkBytes);
-                            const float4 lo = blk[(2 * grp) * BM + row];
-                            const float4 hi = blk[(2 * grp + 1) * BM + row];
-                            acc[j][0] += lo.x; acc[j][1] += lo.y; acc[j][2] += lo.z; acc[j][3] += lo.w;
-                            acc[j][4] += hi.x; acc[j][5] += hi.y; acc[j][6] += hi.z; acc[j][7] += hi.w;
-                        }
-                    }
-                    __syncthreads();
-                }
-#pragma unroll
-                for (int j = 0; j < kUnitsPerThread; ++j) {
-                    const int u = threadIdx.x + j * kThreads;
-                    if (u >= units) continue;
-                    const int cc = u / (BM * 4);
-                    const int row = u % BM;
-                    const int grp = (u / BM) % 4;
-                    const int m = m0 + row;
-                    const int col = n0 + (c0 + cc) * 32 + grp * 8;
-                    if (m >= p.M || col >= p.N) continue;
-                    if (p.y32) {
-                        float4 *d = reinterpret_cast<float4 *>(p.y32 + (int64_t)m * p.ldy + col);
-                        float4 lo = d[0], hi = d[1];
-                        const float *a8 = acc[j];
-                        float o[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) o[e] = kDequant ? a8[unperm(e)] : a8[e];
-                        lo.x += o[0]; lo.y += o[1]; lo.z += o[2]; lo.w += o[3];
-                        hi.x += o[4]; hi.y += o[5]; hi.z += o[6]; hi.w += o[7];
-                        d[0] = lo;
-                        d[1] = hi;
-                        continue;
-                    }
-                    float bv[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) bv[e] = 0.f;
-                    if (p.bias) {
-                        const uint4 braw = __ldg(reinterpret_cast<const uint4 *>(p.bias + col));
-                        const __half *bh = reinterpret_cast<const __half *>(&braw);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) bv[e] = __half2float(bh[e]);
-                    }
-                    __align__(16) __half out[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        out[e] = __float2half_rn((kDequant ? acc[j][unperm(e)] : acc[j][e]) + bv[e]);
-                    *reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.ldy + col) = *reinterpret_cast<const uint4 *>(out);
-                }
-            }
-            // every contributor has counted in: the counter is free for the next call
-            if (threadIdx.x == 0) atomicExch(p.arrive + t, 0u);
         }
     }
     __syncthreads();
@@ -648,6 +526,92 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem_base, kTmemCols);
     }
+}
+
+// Finishing the stream-K tiles: one CTA per (split tile, 32-column chunk),
+// one thread per row of the tile. Each thread adds the fp32 pieces of its row
+// and chunk in contributor order (the same order every call), adds the bias,
+// rounds once and stores (or adds the sum into y32). It is launched right
+// after prefill_kernel as a programmatic dependent: its CTAs may be scheduled
+// while the main grid drains and wait for that grid to complete before they
+// read any partial.
+struct FixupParams {
+    const float *partials;
+    const __half *bias;
+    __half *y;
+    float *y32;
+    int M, N;
+    int64_t ldy;
+    int tiles_m, kiters;
+    int first_tile;         // tile index of stream-K tile 0: dp_waves x the main grid's size
+    int sk_tiles, sk_ctas;
+};
+
+template <bool kDequant>
+__global__ void __launch_bounds__(BM)
+sk_fixup_kernel(const FixupParams p)
+{
+    ptx::wait_prerequisites();
+    const int t = blockIdx.x / (BN / 32);
+    const int c = blockIdx.x % (BN / 32);
+    const int units = p.sk_tiles * p.kiters;
+    const int cf = sk_cta_of(t * p.kiters, units, p.sk_ctas);
+    const int cl = sk_cta_of(t * p.kiters + p.kiters - 1, units, p.sk_ctas);
+    if (cl == cf) return;   // a single contributor took the whole tile and stored it
+    const int tile = p.first_tile + t;
+    const int m = (tile % p.tiles_m) * BM + (int)threadIdx.x;
+    const int col0 = (tile / p.tiles_m) * BN + 32 * c;
+    if (m >= p.M || col0 >= p.N) return;
+    float acc[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+#pragma unroll 2
+    for (int ci = cf; ci <= cl; ++ci) {
+        const int which = (sk_range_begin(ci, units, p.sk_ctas) / p.kiters == t) ? 0 : 1;
+        const float4 *src = reinterpret_cast<const float4 *>(p.partials + (int64_t)(2 * ci + which) * kPartialFloats) +
+                            (c * 8) * BM + threadIdx.x;
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + j * BM);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            acc[4 * j] += v[j].x;
+            acc[4 * j + 1] += v[j].y;
+            acc[4 * j + 2] += v[j].z;
+            acc[4 * j + 3] += v[j].w;
+        }
+    }
+    // accumulator column order -> output column order inside every 8-group
+    float o[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) o[e] = kDequant ? acc[(e & ~7) + unperm(e & 7)] : acc[e];
+    if (p.y32) {
+        float4 *d = reinterpret_cast<float4 *>(p.y32 + (int64_t)m * p.ldy + col0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float4 t4 = d[j];
+            t4.x += o[4 * j];
+            t4.y += o[4 * j + 1];
+            t4.z += o[4 * j + 2];
+            t4.w += o[4 * j + 3];
+            d[j] = t4;
+        }
+        return;
+    }
+    if (p.bias) {
+        __align__(16) __half bh[32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            reinterpret_cast<uint4 *>(bh)[j] = __ldg(reinterpret_cast<const uint4 *>(p.bias + col0) + j);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] += __half2float(bh[e]);
+    }
+    __align__(16) __half out[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) out[e] = __float2half_rn(o[e]);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.ldy + col0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) dst[j] = reinterpret_cast<const uint4 *>(out)[j];
 }
 
 // ---------------------------------------------------------------------------
@@ -691,6 +655,38 @@ int group_rows_per_stage(int64_t g)
     return (int)((BK - 1) / g + 2);
 }
 
+// How a launch covers the tiles. Whole waves of tiles go round-robin over
+// one CTA per SM (neighbouring CTAs share weight tiles in L2). The tiles left
+// over for a last, partial wave are split along k ("stream-K") between up to
+// one CTA per SM, each taking at least kMinUnits k-stages, so that the last
+// wave keeps every SM busy instead of a few; sk_fixup_kernel then sums the
+// pieces of every tile that was split.
+struct Plan {
+    int tiles_m, tiles_n, kiters;
+    int dp_waves, sk_tiles, sk_ctas, ctas;
+    bool split;             // some tile has more than one contributor
+    bool ok;                // sizes within the kernel's index range
+};
+
+Plan plan_tiles(int64_t M, int64_t K, int64_t N, int sms)
+{
+    constexpr int kMinUnits = 8;
+    Plan pl{};
+    pl.tiles_m = (int)((M + BM - 1) / BM);
+    pl.tiles_n = (int)((N + BN - 1) / BN);
+    pl.kiters = (int)((K + BK - 1) / BK);
+    const int64_t n_tiles = (int64_t)pl.tiles_m * pl.tiles_n;
+    pl.dp_waves = (int)(n_tiles / sms);
+    pl.sk_tiles = (int)(n_tiles - (int64_t)pl.dp_waves * sms);
+    const int64_t sk_units = (int64_t)pl.sk_tiles * pl.kiters;
+    pl.sk_ctas = pl.sk_tiles == 0 ? 0
+                 : (int)std::min<int64_t>(sms, std::max<int64_t>(pl.sk_tiles, sk_units / kMinUnits));
+    pl.ctas = pl.dp_waves > 0 ? sms : pl.sk_ctas;
+    pl.split = pl.sk_tiles > 0 && pl.sk_ctas > pl.sk_tiles;
+    pl.ok = sk_units < (int64_t(1) << 31);
+    return pl;
+}
+
 struct LaunchInfo {
     int sms = 0;
     cudaError_t err = cudaSuccess;
@@ -722,23 +718,10 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int6
     const LaunchInfo li = launch_info<kDequant, kWhole>();
     if (li.err != cudaSuccess) return li.err;
     const int M = (int)pr.M, K = (int)pr.K, N = (int)pr.N, g = (int)pr.g;
-    const int tiles_m = (M + BM - 1) / BM;
-    const int tiles_n = (N + BN - 1) / BN;
-    const int kiters = (K + BK - 1) / BK;
-    const int64_t n_tiles = (int64_t)tiles_m * tiles_n;
-    // Whole waves of tiles go round-robin over one CTA per SM (neighbouring
-    // CTAs share weight tiles in L2). The tiles left over for a last, partial
-    // wave are split along k ("stream-K") between up to one CTA per SM, each
-    // taking at least kMinUnits k-stages, so that the last wave keeps every
-    // SM busy instead of a few.
-    constexpr int kMinUnits = 8;
-    const int dp_waves = (int)(n_tiles / li.sms);
-    const int sk_tiles = (int)(n_tiles - (int64_t)dp_waves * li.sms);
-    const int64_t sk_units = (int64_t)sk_tiles * kiters;
-    const int sk_ctas = sk_tiles == 0 ? 0
-                        : (int)std::min<int64_t>(li.sms, std::max<int64_t>(sk_tiles, sk_units / kMinUnits));
-    const int ctas = dp_waves > 0 ? li.sms : sk_ctas;
-    if (sk_units >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+    const Plan pl = plan_tiles(M, K, N, li.sms);
+    if (!pl.ok) return cudaErrorInvalidValue;
+    const int tiles_m = pl.tiles_m, tiles_n = pl.tiles_n, kiters = pl.kiters;
+    const int dp_waves = pl.dp_waves, sk_tiles = pl.sk_tiles, sk_ctas = pl.sk_ctas, ctas = pl.ctas;
 
     CUtensorMap tx, tw, ts, tz;
     const uint64_t ldx = pr.ldx > 0 ? (uint64_t)pr.ldx : (uint64_t)K;
@@ -774,14 +757,38 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int6
     p.tiles_m = tiles_m; p.tiles_n = tiles_n; p.kiters = kiters;
     p.dp_waves = dp_waves; p.sk_tiles = sk_tiles; p.sk_ctas = sk_ctas;
     p.stage_tx = tx_bytes;
-    if (sk_tiles > 0) {
+    const bool split = pl.split;
+    if (split) {
         Scratch sc{};
-        if (!get_scratch(stream, (size_t)2 * sk_ctas * kPartialFloats, (size_t)sk_tiles, &sc))
+        if (!get_scratch(stream, (size_t)2 * sk_ctas * kPartialFloats, 0, &sc))
             return cudaErrorMemoryAllocation;
         p.partials = sc.partials;
-        p.arrive = sc.counters;
     }
     prefill_kernel<kDequant, kWhole><<<ctas, kThreads, Cfg<kDequant>::kSmemBytes, stream>>>(tx, tw, ts, tz, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || !split) return e;
+
+    FixupParams f{};
+    f.partials = p.partials;
+    f.bias = p.bias;
+    f.y = p.y;
+    f.y32 = p.y32;
+    f.M = M; f.N = N; f.ldy = p.ldy;
+    f.tiles_m = tiles_m; f.kiters = kiters;
+    f.first_tile = dp_waves * ctas;
+    f.sk_tiles = sk_tiles; f.sk_ctas = sk_ctas;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(sk_tiles * (BN / 32)));
+    cfg.blockDim = dim3(BM);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, sk_fixup_kernel<kDequant>, f);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -803,6 +810,11 @@ cudaError_t launch_prefill(const Problem &p, cudaStream_t stream)
 cudaError_t launch_gemm_f16(const Problem &p, const void *w16, cudaStream_t stream, int64_t ldy)
 {
     return launch<false, true>(p, w16, stream, ldy);
+}
+
+int prefill_launches(int64_t M, int64_t K, int64_t N, int sms)
+{
+    return plan_tiles(M, K, N, sms).split ? 2 : 1;
 }
 
 } // namespace awq

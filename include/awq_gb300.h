@@ -131,6 +131,19 @@ int awq_path_supported(int64_t M, int64_t K, int64_t N, int64_t group_size, awq_
 int awq_select_path(int64_t M, int64_t K, int64_t N, int64_t group_size);
 
 /*
+ * awq_forward_launches -- how many kernels one awq_linear_forward_path call
+ * (or awq_linear_forward with AWQ_PATH_AUTO) enqueues for this shape on the
+ * current device: 1 on the decode and generic paths; on the prefill path the
+ * persistent kernel plus, when its last partial wave splits tiles along k, the
+ * kernel that sums their pieces; on the dequantise-then-GEMM path, per window,
+ * the dequant kernel and the GEMM core (plus that sum kernel). For callers that
+ * count or budget launches (CUDA graphs). Host-only: reads the current
+ * device's SM count, enqueues nothing. Returns 0 for M == 0 and -1 for an
+ * invalid shape, a path that cannot serve it, or no CUDA device.
+ */
+int awq_forward_launches(int64_t M, int64_t K, int64_t N, int64_t group_size, awq_path_t path);
+
+/*
  * awq_dequant -- unpack and dequantise the packed weights (the per-group
  * dequantisation of the WQLinear page, Description, __init__ bullet 3):
  *   W[k, n] = fp16_rn((q[k, n] - z[k / g, n]) * scales[k / g, n])

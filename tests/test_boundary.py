@@ -187,6 +187,16 @@ def test_automatic_path_follows_the_measured_crossovers(lib):
         assert awq.awq_path_supported(2048, 4100, 12288, -1, path) == 0      # K % 16
 
 
+def test_launch_count_rules_without_a_device(lib):
+    # answers that need no SM count: invalid shapes, M = 0, one-kernel paths
+    assert awq.awq_forward_launches(1, 4096, 12, 128, Path.AUTO) == -1
+    assert awq.awq_forward_launches(-1, 4096, 4096, 128, Path.AUTO) == -1
+    assert awq.awq_forward_launches(0, 4096, 4096, 128, Path.PREFILL) == 0
+    assert awq.awq_forward_launches(1, 4096, 4096, 128, Path.AUTO) == 1        # decode
+    assert awq.awq_forward_launches(7, 4096, 4096, 128, Path.GENERIC) == 1
+    assert awq.awq_forward_launches(1, 4096, 8, -1, Path.PREFILL) == -1       # path cannot serve it
+
+
 def test_layer_checks_on_host():
     qw = torch.zeros((256, 8), dtype=torch.int32)
     qz = torch.zeros((2, 8), dtype=torch.int32)
