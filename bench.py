@@ -57,17 +57,18 @@ NCU_TRAFFIC = {
         },
         "summary": "profiles/decode_kernel_decode-7b.md",
     },
-    # per forward call: the step's 15 launches (3 fused prefill, 6 dequant +
-    # 6 GEMM) over its 9 calls
+    # per forward call: the bytes of the first 21 launches of a step (3 fused
+    # prefill, 3 + 3 dequant / GEMM pairs and their 6 stream-K sums, ...) over
+    # the 9 calls; every launch measured from a cold L2
     "prefill-7b": {
-        "bytes_per_launch": 738613889,
+        "bytes_per_launch": 598955406,
         "sources": {
             "bit_weight_quantized_awq_gb300/csrc/awq_prefill.cu":
-                "98399862eabd04a14d05a650de9a5dd60cf78e569b6864672dfa9b1b3f44370d",
+                "6817f42312a0d483f890b42df66a9d868102e4ac26bd26ab2cb84dce81ad3b8f",
             "bit_weight_quantized_awq_gb300/csrc/awq_tcgen05.cuh":
                 "7583bdc482c3f999df48aafe74db217e2c2055ec6f41779622d85db462730d4a",
             "bit_weight_quantized_awq_gb300/csrc/awq_dequant.cu":
-                "cec5728e91e39c90e73d8a6e73afe2801cc54080a93caa8cb51a8776aec127d4",
+                "6b5733e753c0f9f721ca0c8c31720724d0b67f3db9df404266db62565b469a3e",
             "bit_weight_quantized_awq_gb300/csrc/awq_device.cuh":
                 "3b7d583fc00ea3a961fa897260e5f0245bcdd8b06cb38725fdece027d0787054",
         },
