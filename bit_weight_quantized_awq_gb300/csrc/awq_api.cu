@@ -171,14 +171,16 @@ bool path_fits(const Problem &p, awq_path_t path)
 // Largest M served by the decode kernel when both fast paths fit.
 constexpr int64_t kDecodeMaxM = 32;
 // Dequantising the weights once and running the plain tcgen05 GEMM beats
-// dequantising every weight tile once per 128-token tile inside the fused
-// kernel from M = 2048 on (1.15-1.26x at 2048, 1.35-1.44x at 8192 on the
-// 7B/70B shapes), unless K is so long that the extra pass over fp16
-// weights outweighs the saving (K = 28672 at M = 2048: 0.87x): measured
-// rule M >= 2048 and 8 M >= K.
-constexpr int64_t kDequantGemmMinM = 2048;
+// the fused kernel (which dequantises every weight tile once per 256-token
+// tile) only for long runs of tokens: at M = 8192 by 1.03-1.08x on the 7B
+// and 70B shapes with K <= 11008, while at M = 2048 the fused kernel is
+// 1.1-1.25x faster, and at K = 28672 it wins at M = 8192 too (the fp16
+// weights, 3.6x the packed bytes, no longer stay in L2): measured rule
+// M >= 6144 and K <= 16384.
+constexpr int64_t kDequantGemmMinM = 6144;
+constexpr int64_t kDequantGemmMaxK = 16384;
 
-bool dequant_gemm_pays(const Problem &p) { return p.M >= kDequantGemmMinM && 8 * p.M >= p.K; }
+bool dequant_gemm_pays(const Problem &p) { return p.M >= kDequantGemmMinM && p.K <= kDequantGemmMaxK; }
 
 awq_path_t auto_path(const Problem &p)
 {

@@ -5,16 +5,19 @@
 //   y[m, n] = fp16_rn( sum_k x[m, k] * W[k, n] + bias[n] ),
 //   W[k, n] = fp16_rn((q[k, n] - z[k/g, n]) * s[k/g, n]), fp32 accumulation.
 //
-// Output tile: 128 rows of x (tokens) x 256 output columns; one tcgen05 MMA
-// is M = 128 (tokens) x N = 256 (columns) x K = 16. A persistent grid (one
-// CTA per SM) walks the tiles; inside a CTA, warps are specialised:
+// Output tile: 128 rows of x (tokens) x 256 output columns, or for M > 128
+// 256 rows in two 128-row halves that share every weight tile (MH = 2: the
+// weight tile, and its dequantisation, serve twice the MMA work). One
+// tcgen05 MMA is M = 128 (tokens) x N = 256 (columns) x K = 16. A persistent
+// grid (one CTA per SM) walks the tiles; inside a CTA, warps are specialised:
 //
-//   warp 0      TMA producer: per 64-deep k-stage, the x tile (128 x 64 fp16,
-//               K-major, 128-byte swizzle) and the packed-weight tile
-//               (64 k-rows x 32 words), plus the scale and zero-point rows of
-//               the groups the stage touches, into a 5-stage ring (only what
-//               comes from global memory sits in the ring, so it can be deep
-//               enough to cover the load latency).
+//   warp 0      TMA producer: per 64-deep k-stage, the x tile (128 or 256
+//               x 64 fp16, K-major, 128-byte swizzle) and the packed-weight
+//               tile (64 k-rows x 32 words), plus the scale and zero-point
+//               rows of the groups the stage touches, into a ring of 5 (MH =
+//               1) or 3 (MH = 2) stages (only what comes from global memory
+//               sits in the ring, so it can be deep enough to cover the load
+//               latency).
 //   warps 2-9   dequant: packed words -> fp16 W in one of two B slots,
 //               written directly in the MN-major 128-byte-swizzled layout the
 //               MMA reads as its B operand (one packed word = 8 columns = one
@@ -25,14 +28,16 @@
 //               scales rounds once: exactly fp16_rn((q - z) s). The columns of
 //               every group of 8 are therefore stored as 0 4 1 5 2 6 3 7, and
 //               the epilogue undoes that order.
-//   warp 1      MMA issuer (one thread) and TMEM owner: 4 MMAs per stage into
-//               one of two 256-column fp32 accumulators, tcgen05.commit frees
+//   warp 1      MMA issuer (one thread) and TMEM owner: 4 MMAs per stage and
+//               half into a 256-column fp32 accumulator, tcgen05.commit frees
 //               the stage and the B slot and, at the last stage, hands the
-//               accumulator over.
+//               accumulator over. TMEM holds two accumulators: with MH = 1
+//               tiles alternate between them, with MH = 2 a tile's halves use
+//               one each.
 //   warps 10-13 epilogue: tcgen05.ld of the accumulator (each warp its 32
-//               lanes = 32 tokens), + bias, one rounding to fp16, store. With
-//               two accumulators the epilogue of one tile overlaps the
-//               main loop of the next.
+//               lanes = 32 tokens), + bias, one rounding to fp16, store. The
+//               epilogue of one tile (or half) overlaps the MMAs of the next
+//               tile (or of the other half).
 //
 // A second build of the same kernel (kDequant = false) loads an already
 // dequantised fp16 W with TMA straight into the B layout; it serves
@@ -74,14 +79,20 @@ constexpr int kPBytes = BK * (BN / 8) * 4;      // 8 KB
 // latency) -- and the dequantised B tiles the MMA reads live in a separate
 // pair of slots that the dequant warps fill. Without dequantisation
 // (awq_gemm_f16) a stage is the x tile plus the fp16 B tile, four stages.
-template <bool kDequant>
+// With MH = 2 a tile has 256 rows of x in two 128-row halves that share
+// every B tile (two MMAs per B tile, one per half): the x tile doubles and
+// three stages fit; per MMA cycle an SM then takes in a third less data, and
+// the dequant warps' work per MMA halves.
+template <bool kDequant, int MH>
 struct Cfg {
-    static constexpr int kStages = kDequant ? 5 : 4;
+    static constexpr int kATile = MH * kABytes;                 // x tile: MH x 128 rows
+    static constexpr int kStages = MH == 1 ? (kDequant ? 5 : 4) : 3;
     static constexpr int kAOff = 0;
-    static constexpr int kPOff = kABytes;                       // packed words (dequant)
+    static constexpr int kPOff = kATile;                        // packed words (dequant)
     static constexpr int kSOff = kPOff + kPBytes;               // scale rows (dequant)
     static constexpr int kZOff = kSOff + kMaxGroupRows * BN * 2; // zero-point rows (dequant)
-    static constexpr int kStageBytes = kDequant ? 28 * 1024 : kABytes + kBBytes;
+    static constexpr int kBOff = kATile;                        // fp16 B tile (no dequant)
+    static constexpr int kStageBytes = kDequant ? (MH == 1 ? 28 : 44) * 1024 : kATile + kBBytes;
     static constexpr int kBSlots = kDequant ? 2 : 0;
     static constexpr int kBSlotOff = kStages * kStageBytes;
     static constexpr int kBarOff = kBSlotOff + kBSlots * kBBytes;
@@ -113,12 +124,15 @@ constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
 
 constexpr uint32_t kIdesc = tc::idesc_f16_f32(BM, BN, true);
 
+// Tiles of two 128-row halves from this many rows of x on (see m_halves).
+constexpr int64_t kTwoHalvesMinM = 128;
+
 struct PrefillParams {
     const __half *bias;
     __half *y;
     float *y32;             // if set: y32 += the fp32 sums (no bias, no rounding) instead of y
     unsigned int *status;
-    float *partials;        // [2 * sk_ctas][kPartialFloats] stream-K partial sums
+    float *partials;        // [2 * sk_ctas][MH][kPartialFloats] stream-K partial sums
     int M, K, N, g;
     int64_t ldy;            // elements between rows of y (N, or more for a column window)
     int tiles_m, tiles_n, kiters;
@@ -217,14 +231,15 @@ __device__ __forceinline__ void dequant_word(uint32_t v, const uint32_t (&S)[4],
     h[3] = hmul2_u(hsub2_u((vh & 0x00F000F0u) | 0x54005400u, Z[3]), S[3]);
 }
 
-template <bool kDequant, bool kWhole>
+template <bool kDequant, bool kWhole, int MH>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
                const PrefillParams p)
 {
-    using C = Cfg<kDequant>;
+    using C = Cfg<kDequant, MH>;
     constexpr int kStages = C::kStages;
+    constexpr int BMT = BM * MH;   // rows of x per tile
     extern __shared__ uint8_t smem_raw[];
     // round up to 1024 bytes by offsetting the shared array itself, so that
     // the compiler still knows every derived pointer is a shared address
@@ -287,7 +302,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             for (int si = 0; si < sg.count && ok; ++si) {
                 int tile, kb0, kb1;
                 sg.get(p, si, tile, kb0, kb1);
-                const int m0 = (tile % p.tiles_m) * BM;
+                const int m0 = (tile % p.tiles_m) * BMT;
                 const int n0 = (tile / p.tiles_m) * BN;
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
@@ -308,7 +323,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     } else {
 #pragma unroll
                         for (int a = 0; a < BN / 64; ++a)
-                            ptx::tma_load_2d(st + kABytes + a * kBAtomStride, &tm_w, fb, n0 + 64 * a, k0);
+                            ptx::tma_load_2d(st + C::kBOff + a * kBAtomStride, &tm_w, fb, n0 + 64 * a, k0);
                     }
                     issued = it + 1;
                 }
@@ -328,15 +343,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             for (int si = 0; si < sg.count && ok; ++si, ++acc_it) {
                 int tile, kb0, kb1;
                 sg.get(p, si, tile, kb0, kb1);
-                const int abuf = acc_it & 1;
-                if (!ptx::mbar_wait_bounded(ptx::smem_addr(acc_empty + abuf), ((acc_it >> 1) & 1) ^ 1,
-                                            abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after_sync();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(abuf * BN);
-                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                // accumulator buffers: with MH == 1 tiles alternate between the
+                // two 256-column buffers; with MH == 2 a tile's halves use both
+                const int ab0 = MH == 1 ? (acc_it & 1) : 0;
+                const uint32_t empty_parity = (uint32_t)((MH == 1 ? (acc_it >> 1) : acc_it) & 1) ^ 1u;
+                for (int kb = kb0; kb < kb1 && ok; ++kb, ++it) {
                     const int s = it % kStages;
                     const int b = it % kNB;
                     bool ready = ptx::mbar_wait_bounded(ptx::smem_addr(full + s), (it / kStages) & 1,
@@ -351,17 +362,36 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     tc::fence_after_sync();
                     const uint32_t st = ptx::smem_addr(smem + s * C::kStageBytes);
                     const uint32_t bt = kDequant ? ptx::smem_addr(smem + C::kBSlotOff + b * kBBytes)
-                                                 : st + kABytes;
+                                                 : st + C::kBOff;
 #pragma unroll
-                    for (int kk = 0; kk < BK / kMmaK; ++kk) {
-                        const uint64_t ad = tc::smem_desc_sw128(st + C::kAOff + kk * 32, 16, 1024);
-                        const uint64_t bd = tc::smem_desc_sw128(bt + kk * 2 * kBKGroupStride,
-                                                                kBAtomStride, kBKGroupStride);
-                        tc::mma_f16(d_tmem, ad, bd, kIdesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+                    for (int h = 0; h < MH; ++h) {
+                        // the first stage of a tile waits until the epilogue
+                        // has drained this half's buffer (the other half's
+                        // MMAs may already run)
+                        if (kb == kb0) {
+                            if (!ptx::mbar_wait_bounded(ptx::smem_addr(acc_empty + ab0 + h), empty_parity,
+                                                        abort_flag, p.status)) {
+                                ok = false;
+                                break;
+                            }
+                            tc::fence_after_sync();
+                        }
+                        const uint32_t d_tmem = tmem_base + (uint32_t)((ab0 + h) * BN);
+#pragma unroll
+                        for (int kk = 0; kk < BK / kMmaK; ++kk) {
+                            const uint64_t ad = tc::smem_desc_sw128(st + C::kAOff + h * kABytes + kk * 32, 16, 1024);
+                            const uint64_t bd = tc::smem_desc_sw128(bt + kk * 2 * kBKGroupStride,
+                                                                    kBAtomStride, kBKGroupStride);
+                            tc::mma_f16(d_tmem, ad, bd, kIdesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+                        }
                     }
+                    if (!ok) break;
                     tc::commit(ptx::smem_addr(tfree + s));
                     if (kDequant) tc::commit(ptx::smem_addr(bfree + b));
-                    if (kb == kb1 - 1) tc::commit(ptx::smem_addr(acc_full + abuf));
+                    if (kb == kb1 - 1) {
+#pragma unroll
+                        for (int h = 0; h < MH; ++h) tc::commit(ptx::smem_addr(acc_full + ab0 + h));
+                    }
                 }
             }
             // every MMA this thread issued has completed once `drain` flips
@@ -440,85 +470,93 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                 // TMEM lane quarter this warp may read
         int acc_it = 0;
-        for (int si = 0; si < sg.count; ++si, ++acc_it) {
+        bool ok = true;
+        for (int si = 0; si < sg.count && ok; ++si, ++acc_it) {
             int tile, kb0, kb1;
             sg.get(p, si, tile, kb0, kb1);
-            const int abuf = acc_it & 1;
-            // the decision to go on is taken together by the four warps, which
-            // meet at named barriers below
-            const bool ok = ptx::named_barrier_and(
-                1, kEpilogueThreads,
-                ptx::mbar_wait_bounded(ptx::smem_addr(acc_full + abuf), (acc_it >> 1) & 1, abort_flag, p.status));
-            if (!ok) break;
-            tc::fence_after_sync();
-            const int m0 = (tile % p.tiles_m) * BM;
+            const int ab0 = MH == 1 ? (acc_it & 1) : 0;
+            const uint32_t full_parity = (uint32_t)((MH == 1 ? (acc_it >> 1) : acc_it) & 1);
+            const int m0 = (tile % p.tiles_m) * BMT;
             const int n0 = (tile / p.tiles_m) * BN;
-            const int m = m0 + 32 * q + lane;
-            const uint32_t t_acc = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(abuf * BN);
-            if (kb0 == 0 && kb1 == p.kiters) {
-                // ---- whole tile: + bias, one rounding, store
+            const bool whole = kb0 == 0 && kb1 == p.kiters;
+            // a piece of a stream-K tile goes to this CTA's slot: the first
+            // piece of its range in slot 0, the last in slot 1
+            float *piece = whole ? nullptr
+                                 : p.partials + (int64_t)(2 * (int)blockIdx.x + (si == sg.dp ? 0 : 1)) *
+                                                    (MH * kPartialFloats);
+            for (int h = 0; h < MH; ++h) {
+                const int ab = ab0 + h;
+                // the decision to go on is taken together by the four warps,
+                // which meet at a named barrier
+                ok = ptx::named_barrier_and(
+                    1, kEpilogueThreads,
+                    ptx::mbar_wait_bounded(ptx::smem_addr(acc_full + ab), full_parity, abort_flag, p.status));
+                if (!ok) break;
+                tc::fence_after_sync();
+                const int m = m0 + h * BM + 32 * q + lane;
+                const uint32_t t_acc = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * BN);
+                if (whole) {
+                    // ---- whole tile: + bias, one rounding, store
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t raw[32];
-                    tc::ld_32x32b_x32(t_acc + (uint32_t)(32 * c), raw);
-                    tc::ld_wait();
-                    uint32_t r[32];
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t raw[32];
+                        tc::ld_32x32b_x32(t_acc + (uint32_t)(32 * c), raw);
+                        tc::ld_wait();
+                        uint32_t r[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = kDequant ? raw[(e & ~7) + unperm(e & 7)] : raw[e];
-                    const int col = n0 + 32 * c;
-                    if (col < p.N && m < p.M && p.y32) {
-                        float4 *d = reinterpret_cast<float4 *>(p.y32 + (int64_t)m * p.ldy + col);
+                        for (int e = 0; e < 32; ++e) r[e] = kDequant ? raw[(e & ~7) + unperm(e & 7)] : raw[e];
+                        const int col = n0 + 32 * c;
+                        if (col < p.N && m < p.M && p.y32) {
+                            float4 *d = reinterpret_cast<float4 *>(p.y32 + (int64_t)m * p.ldy + col);
 #pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            float4 t = d[v];
-                            t.x += __uint_as_float(r[4 * v]);
-                            t.y += __uint_as_float(r[4 * v + 1]);
-                            t.z += __uint_as_float(r[4 * v + 2]);
-                            t.w += __uint_as_float(r[4 * v + 3]);
-                            d[v] = t;
+                            for (int v = 0; v < 8; ++v) {
+                                float4 t = d[v];
+                                t.x += __uint_as_float(r[4 * v]);
+                                t.y += __uint_as_float(r[4 * v + 1]);
+                                t.z += __uint_as_float(r[4 * v + 2]);
+                                t.w += __uint_as_float(r[4 * v + 3]);
+                                d[v] = t;
+                            }
+                        } else if (col < p.N && m < p.M) {
+                            __align__(16) __half out[32];
+                            if (p.bias) {
+                                __align__(16) __half bh[32];
+#pragma unroll
+                                for (int v = 0; v < 4; ++v)
+                                    reinterpret_cast<uint4 *>(bh)[v] = __ldg(reinterpret_cast<const uint4 *>(p.bias + col) + v);
+#pragma unroll
+                                for (int e = 0; e < 32; ++e)
+                                    out[e] = __float2half_rn(__uint_as_float(r[e]) + __half2float(bh[e]));
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) out[e] = __float2half_rn(__uint_as_float(r[e]));
+                            }
+                            uint4 *dst = reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.ldy + col);
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) dst[v] = reinterpret_cast<const uint4 *>(out)[v];
                         }
-                    } else if (col < p.N && m < p.M) {
-                        __align__(16) __half out[32];
-                        if (p.bias) {
-                            __align__(16) __half bh[32];
+                    }
+                } else {
+                    // ---- a piece of a stream-K tile: store the fp32 partial
+                    //      of this half; sk_fixup_kernel, launched after this
+                    //      grid, sums the pieces of every split tile
+                    float *mine = piece + (int64_t)h * kPartialFloats;
+#pragma unroll 1
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t raw[32];
+                        tc::ld_32x32b_x32(t_acc + (uint32_t)(32 * c), raw);
+                        tc::ld_wait();
+                        if (m < p.M) {
 #pragma unroll
-                            for (int v = 0; v < 4; ++v)
-                                reinterpret_cast<uint4 *>(bh)[v] = __ldg(reinterpret_cast<const uint4 *>(p.bias + col) + v);
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                out[e] = __float2half_rn(__uint_as_float(r[e]) + __half2float(bh[e]));
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) out[e] = __float2half_rn(__uint_as_float(r[e]));
+                            for (int v = 0; v < 8; ++v)
+                                reinterpret_cast<uint4 *>(mine)[(c * 8 + v) * BM + 32 * q + lane] =
+                                    make_uint4(raw[4 * v], raw[4 * v + 1], raw[4 * v + 2], raw[4 * v + 3]);
                         }
-                        uint4 *dst = reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.ldy + col);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) dst[v] = reinterpret_cast<const uint4 *>(out)[v];
                     }
                 }
                 tc::fence_before_sync();
-                ptx::mbar_arrive(ptx::smem_addr(acc_empty + abuf));
-                continue;
+                ptx::mbar_arrive(ptx::smem_addr(acc_empty + ab));
             }
-            // ---- a piece of a stream-K tile: store the fp32 partial (first
-            //      piece of this CTA's range in slot 0, last in slot 1) and
-            //      free the accumulator; sk_fixup_kernel, launched after this
-            //      grid, sums the pieces of every split tile.
-            float *mine = p.partials + (int64_t)(2 * (int)blockIdx.x + (si == sg.dp ? 0 : 1)) * kPartialFloats;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t raw[32];
-                tc::ld_32x32b_x32(t_acc + (uint32_t)(32 * c), raw);
-                tc::ld_wait();
-                if (m < p.M) {
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        reinterpret_cast<uint4 *>(mine)[(c * 8 + v) * BM + 32 * q + lane] =
-                            make_uint4(raw[4 * v], raw[4 * v + 1], raw[4 * v + 2], raw[4 * v + 3]);
-                }
-            }
-            tc::fence_before_sync();
-            ptx::mbar_arrive(ptx::smem_addr(acc_empty + abuf));
         }
     }
     __syncthreads();
@@ -528,8 +566,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     }
 }
 
-// Finishing the stream-K tiles: one CTA per (split tile, 32-column chunk),
-// one thread per row of the tile. Each thread adds the fp32 pieces of its row
+// Finishing the stream-K tiles: one CTA per (split tile, 128-row half,
+// 32-column chunk), one thread per row. Each thread adds the fp32 pieces of its row
 // and chunk in contributor order (the same order every call), adds the bias,
 // rounds once and stores (or adds the sum into y32). It is launched right
 // after prefill_kernel as a programmatic dependent: its CTAs may be scheduled
@@ -547,19 +585,20 @@ struct FixupParams {
     int sk_tiles, sk_ctas;
 };
 
-template <bool kDequant>
+template <bool kDequant, int MH>
 __global__ void __launch_bounds__(BM)
 sk_fixup_kernel(const FixupParams p)
 {
     ptx::wait_prerequisites();
-    const int t = blockIdx.x / (BN / 32);
+    const int t = blockIdx.x / (MH * (BN / 32));
+    const int h = (blockIdx.x / (BN / 32)) % MH;
     const int c = blockIdx.x % (BN / 32);
     const int units = p.sk_tiles * p.kiters;
     const int cf = sk_cta_of(t * p.kiters, units, p.sk_ctas);
     const int cl = sk_cta_of(t * p.kiters + p.kiters - 1, units, p.sk_ctas);
     if (cl == cf) return;   // a single contributor took the whole tile and stored it
     const int tile = p.first_tile + t;
-    const int m = (tile % p.tiles_m) * BM + (int)threadIdx.x;
+    const int m = (tile % p.tiles_m) * (BM * MH) + h * BM + (int)threadIdx.x;
     const int col0 = (tile / p.tiles_m) * BN + 32 * c;
     if (m >= p.M || col0 >= p.N) return;
     float acc[32];
@@ -568,7 +607,8 @@ sk_fixup_kernel(const FixupParams p)
 #pragma unroll 2
     for (int ci = cf; ci <= cl; ++ci) {
         const int which = (sk_range_begin(ci, units, p.sk_ctas) / p.kiters == t) ? 0 : 1;
-        const float4 *src = reinterpret_cast<const float4 *>(p.partials + (int64_t)(2 * ci + which) * kPartialFloats) +
+        const float4 *src = reinterpret_cast<const float4 *>(p.partials + ((int64_t)(2 * ci + which) * MH + h) *
+                                                                               kPartialFloats) +
                             (c * 8) * BM + threadIdx.x;
         float4 v[8];
 #pragma unroll
@@ -668,11 +708,11 @@ struct Plan {
     bool ok;                // sizes within the kernel's index range
 };
 
-Plan plan_tiles(int64_t M, int64_t K, int64_t N, int sms)
+Plan plan_tiles(int64_t M, int64_t K, int64_t N, int sms, int mh)
 {
     constexpr int kMinUnits = 8;
     Plan pl{};
-    pl.tiles_m = (int)((M + BM - 1) / BM);
+    pl.tiles_m = (int)((M + BM * mh - 1) / (BM * mh));
     pl.tiles_n = (int)((N + BN - 1) / BN);
     pl.kiters = (int)((K + BK - 1) / BK);
     const int64_t n_tiles = (int64_t)pl.tiles_m * pl.tiles_n;
@@ -692,7 +732,7 @@ struct LaunchInfo {
     cudaError_t err = cudaSuccess;
 };
 
-template <bool kDequant, bool kWhole>
+template <bool kDequant, bool kWhole, int MH>
 LaunchInfo launch_info()
 {
     static std::mutex mu;
@@ -704,30 +744,30 @@ LaunchInfo launch_info()
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(dev);
     if (it != cache.end()) return it->second;
-    li.err = cudaFuncSetAttribute(prefill_kernel<kDequant, kWhole>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  Cfg<kDequant>::kSmemBytes);
+    li.err = cudaFuncSetAttribute(prefill_kernel<kDequant, kWhole, MH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  Cfg<kDequant, MH>::kSmemBytes);
     if (li.err == cudaSuccess)
         li.err = cudaDeviceGetAttribute(&li.sms, cudaDevAttrMultiProcessorCount, dev);
     if (li.err == cudaSuccess) cache[dev] = li;
     return li;
 }
 
-template <bool kDequant, bool kWhole>
+template <bool kDequant, bool kWhole, int MH>
 cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int64_t ldy)
 {
-    const LaunchInfo li = launch_info<kDequant, kWhole>();
+    const LaunchInfo li = launch_info<kDequant, kWhole, MH>();
     if (li.err != cudaSuccess) return li.err;
     const int M = (int)pr.M, K = (int)pr.K, N = (int)pr.N, g = (int)pr.g;
-    const Plan pl = plan_tiles(M, K, N, li.sms);
+    const Plan pl = plan_tiles(M, K, N, li.sms, MH);
     if (!pl.ok) return cudaErrorInvalidValue;
     const int tiles_m = pl.tiles_m, tiles_n = pl.tiles_n, kiters = pl.kiters;
     const int dp_waves = pl.dp_waves, sk_tiles = pl.sk_tiles, sk_ctas = pl.sk_ctas, ctas = pl.ctas;
 
     CUtensorMap tx, tw, ts, tz;
     const uint64_t ldx = pr.ldx > 0 ? (uint64_t)pr.ldx : (uint64_t)K;
-    bool ok = make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.x, K, M, ldx * 2, BK, BM,
+    bool ok = make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.x, K, M, ldx * 2, BK, BM * MH,
                           CU_TENSOR_MAP_SWIZZLE_128B);
-    uint32_t tx_bytes = kABytes;
+    uint32_t tx_bytes = kABytes * MH;
     if (kDequant) {
         const int R = group_rows_per_stage(g);
         ok = ok &&
@@ -760,11 +800,11 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int6
     const bool split = pl.split;
     if (split) {
         Scratch sc{};
-        if (!get_scratch(stream, (size_t)2 * sk_ctas * kPartialFloats, 0, &sc))
+        if (!get_scratch(stream, (size_t)2 * sk_ctas * MH * kPartialFloats, 0, &sc))
             return cudaErrorMemoryAllocation;
         p.partials = sc.partials;
     }
-    prefill_kernel<kDequant, kWhole><<<ctas, kThreads, Cfg<kDequant>::kSmemBytes, stream>>>(tx, tw, ts, tz, p);
+    prefill_kernel<kDequant, kWhole, MH><<<ctas, kThreads, Cfg<kDequant, MH>::kSmemBytes, stream>>>(tx, tw, ts, tz, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !split) return e;
 
@@ -778,7 +818,7 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int6
     f.first_tile = dp_waves * ctas;
     f.sk_tiles = sk_tiles; f.sk_ctas = sk_ctas;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)(sk_tiles * (BN / 32)));
+    cfg.gridDim = dim3((unsigned)(sk_tiles * MH * (BN / 32)));
     cfg.blockDim = dim3(BM);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -787,7 +827,7 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int6
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, sk_fixup_kernel<kDequant>, f);
+    e = cudaLaunchKernelEx(&cfg, sk_fixup_kernel<kDequant, MH>, f);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -800,21 +840,33 @@ bool prefill_supported(int64_t M, int64_t K, int64_t N, int64_t g)
            K <= (int64_t(1) << 30) && N <= (int64_t(1) << 30);
 }
 
+// 128-row halves per tile: two (256-row tiles sharing every B tile) once M
+// fills them, else one.
+int m_halves(int64_t M)
+{
+    return M > kTwoHalvesMinM ? 2 : 1;
+}
+
 cudaError_t launch_prefill(const Problem &p, cudaStream_t stream)
 {
     if (!prefill_supported(p.M, p.K, p.N, p.g)) return cudaErrorInvalidValue;
     // g % 64 == 0: every 64-row stage lies in one group
-    return p.g % BK == 0 ? launch<true, true>(p, nullptr, stream, 0) : launch<true, false>(p, nullptr, stream, 0);
+    if (m_halves(p.M) == 2)
+        return p.g % BK == 0 ? launch<true, true, 2>(p, nullptr, stream, 0)
+                             : launch<true, false, 2>(p, nullptr, stream, 0);
+    return p.g % BK == 0 ? launch<true, true, 1>(p, nullptr, stream, 0)
+                         : launch<true, false, 1>(p, nullptr, stream, 0);
 }
 
 cudaError_t launch_gemm_f16(const Problem &p, const void *w16, cudaStream_t stream, int64_t ldy)
 {
-    return launch<false, true>(p, w16, stream, ldy);
+    return m_halves(p.M) == 2 ? launch<false, true, 2>(p, w16, stream, ldy)
+                              : launch<false, true, 1>(p, w16, stream, ldy);
 }
 
 int prefill_launches(int64_t M, int64_t K, int64_t N, int sms)
 {
-    return plan_tiles(M, K, N, sms).split ? 2 : 1;
+    return plan_tiles(M, K, N, sms, m_halves(M)).split ? 2 : 1;
 }
 
 } // namespace awq

@@ -96,7 +96,7 @@ typedef enum {
  *
  * Kernel family (AWQ_PATH_AUTO, chosen from measurements on GB300): the
  * decode kernel for M <= 32; the fused tcgen05 prefill kernel for larger M;
- * for M >= 2048 with 8 M >= K, the weights dequantised once into a
+ * for M >= 6144 with K <= 16384, the weights dequantised once into a
  * per-stream scratch area (windows of at most 256 MB of fp16, allocated on
  * first use) and the same kernel's tcgen05 GEMM core; the generic kernel
  * for shapes the others do not take.

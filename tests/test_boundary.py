@@ -175,13 +175,13 @@ def test_path_support_rules(lib):
 
 
 def test_automatic_path_follows_the_measured_crossovers(lib):
-    # decode through 32 tokens, the fused tcgen05 kernel up to 2047, then the
-    # weights dequantised once and the plain tcgen05 GEMM (when 8 M >= K)
-    for M, want in [(1, Path.DECODE), (32, Path.DECODE), (33, Path.PREFILL), (2047, Path.PREFILL),
-                    (2048, Path.DEQUANT_GEMM), (8192, Path.DEQUANT_GEMM)]:
+    # decode through 32 tokens, the fused tcgen05 kernel up to 6143, then the
+    # weights dequantised once and the plain tcgen05 GEMM (when K <= 16384)
+    for M, want in [(1, Path.DECODE), (32, Path.DECODE), (33, Path.PREFILL), (2048, Path.PREFILL),
+                    (6143, Path.PREFILL), (6144, Path.DEQUANT_GEMM), (8192, Path.DEQUANT_GEMM)]:
         assert awq.awq_select_path(M, 4096, 12288, 128) == want, M
-    assert awq.awq_select_path(2048, 28672, 8192, 128) == Path.PREFILL
-    assert awq.awq_select_path(8192, 28672, 8192, 128) == Path.DEQUANT_GEMM
+    assert awq.awq_select_path(8192, 16384, 8192, 128) == Path.DEQUANT_GEMM
+    assert awq.awq_select_path(8192, 28672, 8192, 128) == Path.PREFILL
     for path in (Path.PREFILL, Path.DEQUANT_GEMM):
         assert awq.awq_path_supported(2048, 4096, 12288, 128, path) == 1
         assert awq.awq_path_supported(2048, 4100, 12288, -1, path) == 0      # K % 16

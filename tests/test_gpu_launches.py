@@ -17,7 +17,8 @@ CASES = [
     (64, 8192, 10240, 128, Path.AUTO),        # fused prefill, every tile split
     (512, 4096, 12288, 128, Path.PREFILL),    # one wave + split tiles
     (128, 4096, 38912, 128, Path.PREFILL),    # 152 whole tiles: no split
-    (2048, 4096, 12288, 128, Path.AUTO),      # dequant + GEMM + sum
+    (2048, 4096, 12288, 128, Path.AUTO),      # fused, 256-row tiles
+    (8192, 4096, 12288, 128, Path.AUTO),      # dequant + GEMM
     (2048, 11008, 4096, 128, Path.DEQUANT_GEMM),
 ]
 
@@ -58,7 +59,8 @@ def test_kernels_per_call_match_the_plan(M, K, N, g, path):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     used = Path(awq.awq_select_path(M, K, N, g)) if path == Path.AUTO else path
     if used in (Path.PREFILL, Path.DEQUANT_GEMM):
-        tiles = -(-M // 128) * -(-N // 256)
+        rows = 128 if M <= 128 else 256      # 128-row tiles, or two halves of 128 rows
+        tiles = -(-M // rows) * -(-N // 256)
         assert (n_sum == 1) == (tiles % sms != 0), (tiles, sms, names)
     else:
         assert n_sum == 0
