@@ -13,7 +13,7 @@ step, more than twice the 129 MB L2), so each call reads its weights cold.
     python bench.py [--steps K] [--warmup W] [--impl native|reference]
     python bench.py --sweep --workload all    # per-problem table, every path
     python bench.py --sweep --workload quantize   # awq_quantize_rtn / awq_pack GB/s
-    python bench.py --sweep --workload gidx       # awq_linear_forward_gidx TFLOP/s
+    python bench.py --sweep --workload gidx       # g_idx forward: table and sorted (act-order) forms
     python bench.py --sweep --workload shard      # column/row-sharded layer on one GPU
 
 Timing: one CUDA graph per step (its launches each bracketed by external
@@ -57,18 +57,18 @@ NCU_TRAFFIC = {
         },
         "summary": "profiles/decode_kernel_decode-7b.md",
     },
-    # per forward call: the bytes of the first 21 launches of a step (3 fused
-    # prefill, 3 + 3 dequant / GEMM pairs and their 6 stream-K sums, ...) over
-    # the 9 calls; every launch measured from a cold L2
+    # per forward call: the bytes of one step's 21 launches (3 fused + sum,
+    # 3 fused + sum, 3 dequant + GEMM + sum) over its 9 calls, every launch
+    # measured from a cold L2
     "prefill-7b": {
-        "bytes_per_launch": 598955406,
+        "bytes_per_launch": 526029028,
         "sources": {
             "bit_weight_quantized_awq_gb300/csrc/awq_prefill.cu":
-                "6817f42312a0d483f890b42df66a9d868102e4ac26bd26ab2cb84dce81ad3b8f",
+                "b723f8238cf5bf1b904745808ff8d80e350ca5c77433384a8bf8e9bc15491070",
             "bit_weight_quantized_awq_gb300/csrc/awq_tcgen05.cuh":
                 "7583bdc482c3f999df48aafe74db217e2c2055ec6f41779622d85db462730d4a",
             "bit_weight_quantized_awq_gb300/csrc/awq_dequant.cu":
-                "6b5733e753c0f9f721ca0c8c31720724d0b67f3db9df404266db62565b469a3e",
+                "ab8c5a1fb918217b860b7c18914bc103a104ee75b046b6efa1498301bc0d4370",
             "bit_weight_quantized_awq_gb300/csrc/awq_device.cuh":
                 "3b7d583fc00ea3a961fa897260e5f0245bcdd8b06cb38725fdece027d0787054",
         },
@@ -678,9 +678,12 @@ def run_quantize_sweep(args, device, peaks):
 
 
 def run_gidx_sweep(args, device, peaks):
-    """awq_linear_forward_gidx (act-order table: each group holds 128 rows,
-    scattered by a permutation) on 7B-class shapes: TFLOP/s and the binding
-    roofline fraction, back-to-back launches over two weight copies."""
+    """The g_idx variant with an act-order table (each group holds 128 rows,
+    scattered by a permutation) on 7B-class shapes, two ways: the table read
+    as is (awq_linear_forward_gidx: the layer dequantised whole, then the
+    GEMM core) and the rows sorted by group once (awq_linear_forward_sorted:
+    x's columns gathered, then the grouped kernels). TFLOP/s and the binding
+    roofline fraction, back-to-back calls over two weight copies."""
     import bit_weight_quantized_awq_gb300 as awq
     awq.load_library()
     out = open(args.sweep_out, "w") if args.sweep_out else None
@@ -697,40 +700,49 @@ def run_gidx_sweep(args, device, peaks):
                 sc = (torch.rand((G, N), device=device, generator=gen) * 9e-3 + 1e-3).half()
                 perm = torch.randperm(K, device=device, generator=gen)
                 gi = (torch.arange(K, device=device) // 128)[perm].to(torch.int32).contiguous()
-                sets.append((qw, qz, sc, gi))
+                with torch.cuda.stream(stream):
+                    qs, sperm, _ = awq.prepare_act_order(qw, gi, G)
+                sets.append((qw, qz, sc, gi, qs, sperm))
             x = torch.randn((M, K), device=device, generator=gen).half()
             y = torch.empty((M, N), device=device, dtype=torch.float16)
-            fn = lambda st: awq.awq_linear_forward_gidx(x.data_ptr(), st[0].data_ptr(), st[1].data_ptr(),
-                                                        st[2].data_ptr(), st[3].data_ptr(), None,
-                                                        y.data_ptr(), M, K, N, G, h)
-            with torch.cuda.stream(stream):
-                for st in sets:
-                    if fn(st) != 0:
-                        raise RuntimeError(f"gidx forward failed on {(M, K, N)}")
-            stream.synchronize()
-            reps = max(3, min(50, int(2e-3 / max(1e-7, flops(M, K, N) / 1e15))))
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
-                for r in range(reps):
-                    fn(sets[r % 2])
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                graph.replay()
+            forms = {
+                "table": lambda st: awq.awq_linear_forward_gidx(x.data_ptr(), st[0].data_ptr(), st[1].data_ptr(),
+                                                                st[2].data_ptr(), st[3].data_ptr(), None,
+                                                                y.data_ptr(), M, K, N, G, h),
+                "sorted": lambda st: awq.awq_linear_forward_sorted(x.data_ptr(), st[5].data_ptr(), st[4].data_ptr(),
+                                                                   st[1].data_ptr(), st[2].data_ptr(), None,
+                                                                   y.data_ptr(), M, K, N, 128, h),
+            }
+            for form, fn in forms.items():
+                with torch.cuda.stream(stream):
+                    for st in sets:
+                        if fn(st) != 0:
+                            raise RuntimeError(f"gidx forward ({form}) failed on {(M, K, N)}")
                 stream.synchronize()
-                e0.record(stream)
-                graph.replay()
-                e1.record(stream)
-            torch.cuda.synchronize(device)
-            t = e0.elapsed_time(e1) / 1e3 / reps
-            row = {"workload": "gidx", "M": M, "K": K, "N": N, "G": G, "us": t * 1e6,
-                   "tflops": flops(M, K, N) / t / 1e12,
-                   "tc_frac": flops(M, K, N) / t / 1e12 / peaks["bf16_tflops"],
-                   "hbm_frac": algo_bytes(M, K, N, 128, False) / t / 1e9 / peaks["hbm_gbs"]}
-            print(json.dumps(row), file=sys.stderr, flush=True)
-            if out:
-                out.write(json.dumps(row) + "\n")
-                out.flush()
-            del graph, sets
+                reps = max(3, min(50, int(2e-3 / max(1e-7, flops(M, K, N) / 1e15))))
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=stream):
+                    for r in range(reps):
+                        fn(sets[r % 2])
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    graph.replay()
+                    stream.synchronize()
+                    e0.record(stream)
+                    graph.replay()
+                    e1.record(stream)
+                torch.cuda.synchronize(device)
+                t = e0.elapsed_time(e1) / 1e3 / reps
+                row = {"workload": "gidx", "form": form, "M": M, "K": K, "N": N, "G": G, "us": t * 1e6,
+                       "tflops": flops(M, K, N) / t / 1e12,
+                       "tc_frac": flops(M, K, N) / t / 1e12 / peaks["bf16_tflops"],
+                       "hbm_frac": algo_bytes(M, K, N, 128, False) / t / 1e9 / peaks["hbm_gbs"]}
+                print(json.dumps(row), file=sys.stderr, flush=True)
+                if out:
+                    out.write(json.dumps(row) + "\n")
+                    out.flush()
+                del graph
+            del sets
             torch.cuda.empty_cache()
     if out:
         out.close()

@@ -20,11 +20,14 @@ from ._binding import (  # noqa: F401
     awq_linear_forward,
     awq_linear_forward_decode_noalloc,
     awq_finish_rows,
+    awq_gidx_sort,
     awq_linear_forward_gidx,
+    awq_linear_forward_sorted,
     awq_linear_forward_rows,
     awq_linear_forward_path,
     awq_pack,
     awq_path_supported,
+    awq_permute_rows,
     awq_quantize_rtn,
     awq_select_path,
     awq_forward_launches,
@@ -32,5 +35,5 @@ from ._binding import (  # noqa: F401
     awq_status_string,
     load_library,
 )
-from .layer import (AWQLinear, dequant, dequant_gidx, linear_forward, linear_forward_gidx,  # noqa: F401
-                    pack, quantize_rtn)
+from .layer import (AWQLinear, dequant, dequant_gidx, gidx_sort, linear_forward,  # noqa: F401
+                    linear_forward_gidx, linear_forward_sorted, pack, prepare_act_order, quantize_rtn)

@@ -34,6 +34,9 @@ EXPORTED = (
     "awq_linear_forward_gidx",
     "awq_linear_forward_rows",
     "awq_finish_rows",
+    "awq_gidx_sort",
+    "awq_permute_rows",
+    "awq_linear_forward_sorted",
 )
 
 
@@ -107,6 +110,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.awq_linear_forward_gidx.restype = _INT
         lib.awq_linear_forward_rows.argtypes = [_P, _I64, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]
         lib.awq_linear_forward_rows.restype = _INT
+        lib.awq_gidx_sort.argtypes = [_P, _I64, _I64, _P]
+        lib.awq_gidx_sort.restype = _INT
+        lib.awq_permute_rows.argtypes = [_P, _P, _P, _I64, _I64, _P]
+        lib.awq_permute_rows.restype = _INT
+        lib.awq_linear_forward_sorted.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]
+        lib.awq_linear_forward_sorted.restype = _INT
         lib.awq_finish_rows.argtypes = [_P, _P, _P, _I64, _I64, _P]
         lib.awq_finish_rows.restype = _INT
         lib.awq_pack.argtypes = [_P, _P, _I64, _I64, _P]
@@ -159,6 +168,20 @@ def awq_dequant_gidx(qweight, qzeros, scales, g_idx, W, K, N, G, stream) -> int:
 def awq_linear_forward_gidx(x, qweight, qzeros, scales, g_idx, bias, y, M, K, N, G, stream) -> int:
     return load_library().awq_linear_forward_gidx(x, qweight, qzeros, scales, g_idx, bias, y,
                                                   M, K, N, G, stream)
+
+
+def awq_gidx_sort(g_idx, K, G, perm) -> int:
+    return load_library().awq_gidx_sort(g_idx, K, G, perm)
+
+
+def awq_permute_rows(qweight, perm, qweight_sorted, K, N, stream) -> int:
+    return load_library().awq_permute_rows(qweight, perm, qweight_sorted, K, N, stream)
+
+
+def awq_linear_forward_sorted(x, perm, qweight_sorted, qzeros, scales, bias, y, M, K, N, group_size,
+                              stream) -> int:
+    return load_library().awq_linear_forward_sorted(x, perm, qweight_sorted, qzeros, scales, bias, y,
+                                                    M, K, N, group_size, stream)
 
 
 def awq_linear_forward_rows(x, ldx, qweight, qzeros, scales, y32, M, K, N, group_size, stream) -> int:

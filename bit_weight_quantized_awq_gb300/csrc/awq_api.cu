@@ -37,6 +37,8 @@ struct ScratchEntry {
     size_t n_counters = 0;
     void *w16 = nullptr;           // dequantised weights of the g_idx forward
     size_t w16_bytes = 0;
+    void *xs = nullptr;            // activations in sorted row order (act-order forward)
+    size_t xs_bytes = 0;
 };
 std::map<std::pair<int, cudaStream_t>, ScratchEntry> g_scratch;
 
@@ -100,28 +102,44 @@ bool get_scratch(cudaStream_t stream, size_t partial_floats, size_t n_counters, 
     return true;
 }
 
-bool get_w16_scratch(cudaStream_t stream, size_t bytes, void **out)
+namespace {
+
+// Grows one byte area of this (device, stream)'s scratch to at least `bytes`.
+bool grow_area(cudaStream_t stream, size_t bytes, void *ScratchEntry::*ptr, size_t ScratchEntry::*cap,
+               void **out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     std::lock_guard<std::mutex> lock(g_mutex);
     ScratchEntry &e = g_scratch[std::make_pair(dev, stream)];
-    if (e.w16_bytes < bytes) {
+    if (e.*cap < bytes) {
         // the old area may still be read by work queued on this stream
-        if (e.w16) {
+        if (e.*ptr) {
             cudaStreamSynchronize(stream);
-            cudaFree(e.w16);
-            e.w16 = nullptr;
-            e.w16_bytes = 0;
+            cudaFree(e.*ptr);
+            e.*ptr = nullptr;
+            e.*cap = 0;
         }
-        if (cudaMalloc(&e.w16, bytes) != cudaSuccess) {
-            e.w16 = nullptr;
+        if (cudaMalloc(&(e.*ptr), bytes) != cudaSuccess) {
+            e.*ptr = nullptr;
             return false;
         }
-        e.w16_bytes = bytes;
+        e.*cap = bytes;
     }
-    *out = e.w16;
+    *out = e.*ptr;
     return true;
+}
+
+} // namespace
+
+bool get_w16_scratch(cudaStream_t stream, size_t bytes, void **out)
+{
+    return grow_area(stream, bytes, &ScratchEntry::w16, &ScratchEntry::w16_bytes, out);
+}
+
+bool get_xs_scratch(cudaStream_t stream, size_t bytes, void **out)
+{
+    return grow_area(stream, bytes, &ScratchEntry::xs, &ScratchEntry::xs_bytes, out);
 }
 
 // Drops the counters of every scratch area on this device so that the next
@@ -381,6 +399,65 @@ awq_status_t awq_linear_forward_gidx(const void *x, const int32_t *qweight, cons
     return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
 }
 
+awq_status_t awq_gidx_sort(const int32_t *g_idx, int64_t K, int64_t G, int32_t *perm)
+{
+    if (K <= 0 || G <= 0 || K % G != 0 || K > (int64_t(1) << 30) || !g_idx || !perm)
+        return AWQ_ERR_INVALID_ARG;
+    const int64_t g = K / G;
+    std::vector<int64_t> next((size_t)G, 0);
+    for (int64_t k = 0; k < K; ++k) {
+        const int64_t gi = g_idx[k];
+        if (gi < 0 || gi >= G || next[(size_t)gi] == g) return AWQ_ERR_INVALID_ARG;
+        ++next[(size_t)gi];
+    }
+    // every group holds exactly g rows: sorted row gi * g + j is the j-th
+    // row of group gi in the original order (a stable counting sort)
+    for (int64_t gi = 0; gi < G; ++gi) next[(size_t)gi] = gi * g;
+    for (int64_t k = 0; k < K; ++k) perm[next[(size_t)g_idx[k]]++] = (int32_t)k;
+    return AWQ_OK;
+}
+
+awq_status_t awq_permute_rows(const int32_t *qweight, const int32_t *perm, int32_t *qweight_sorted,
+                              int64_t K, int64_t N, awq_stream_t stream)
+{
+    if (K <= 0 || N <= 0 || N % 32 != 0 || K > (int64_t(1) << 30)) return AWQ_ERR_INVALID_ARG;
+    if (!qweight || !perm || !qweight_sorted) return AWQ_ERR_INVALID_ARG;
+    if (!aligned16(qweight) || !aligned16(perm) || !aligned16(qweight_sorted)) return AWQ_ERR_MISALIGNED;
+    cudaError_t e = awq::launch_gather_rows(qweight, perm, qweight_sorted, K, N / 8,
+                                            reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+}
+
+awq_status_t awq_linear_forward_sorted(const void *x, const int32_t *perm, const int32_t *qweight_sorted,
+                                       const int32_t *qzeros, const void *scales, const void *bias,
+                                       void *y, int64_t M, int64_t K, int64_t N, int64_t group_size,
+                                       awq_stream_t stream)
+{
+    int64_t g = 0;
+    if (M < 0) return AWQ_ERR_INVALID_ARG;
+    awq_status_t st = check_shape(K, N, group_size, &g);
+    if (st != AWQ_OK) return st;
+    if (K % 8 != 0) return AWQ_ERR_INVALID_ARG;
+    if (M == 0) return AWQ_OK;
+    if (!x || !perm || !qweight_sorted || !qzeros || !scales || !y) return AWQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(perm) || !aligned16(qweight_sorted) || !aligned16(qzeros) ||
+        !aligned16(scales) || !aligned16(y) || (bias && !aligned16(bias)))
+        return AWQ_ERR_MISALIGNED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    Problem p{x, qweight_sorted, qzeros, scales, bias, y, M, K, N, g, K / g};
+    if (auto_path(p) == AWQ_PATH_DEQUANT_GEMM) {
+        // the weights are dequantised anyway: put their rows back in the
+        // original order while doing so, and leave x as it is
+        p.row_perm = perm;
+        return awq::launch_dequant_gemm(p, s) == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+    }
+    void *xs = nullptr;
+    if (!awq::get_xs_scratch(s, (size_t)M * (size_t)K * 2, &xs)) return AWQ_ERR_CUDA;
+    if (awq::launch_gather_cols(x, K, perm, xs, M, K, s) != cudaSuccess) return AWQ_ERR_CUDA;
+    return awq_linear_forward_path(xs, qweight_sorted, qzeros, scales, bias, y, M, K, N, group_size, stream,
+                                   AWQ_PATH_AUTO);
+}
+
 awq_status_t awq_pack(const uint8_t *codes, int32_t *packed, int64_t rows, int64_t cols,
                       awq_stream_t stream)
 {
@@ -454,6 +531,7 @@ void awq_shutdown(void)
         if (kv.second.partials) cudaFree(kv.second.partials);
         if (kv.second.counters) cudaFree(kv.second.counters);
         if (kv.second.w16) cudaFree(kv.second.w16);
+        if (kv.second.xs) cudaFree(kv.second.xs);
     }
     awq::g_scratch.clear();
     cudaSetDevice(prev);

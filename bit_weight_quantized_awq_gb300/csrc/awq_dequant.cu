@@ -18,14 +18,27 @@ namespace {
 __global__ void __launch_bounds__(256)
 dequant_kernel(const uint32_t *__restrict__ qweight, const uint32_t *__restrict__ qzeros,
                const __half *__restrict__ scales, __half *__restrict__ W,
-               int64_t K, int64_t words, int64_t g, int64_t word0, int64_t wwords)
+               int64_t K, int64_t words, int64_t g, int64_t word0, int64_t wwords,
+               const int32_t *__restrict__ row_out, unsigned int *status)
 {
-    // output: words word0 .. word0 + wwords - 1 of every row, as a [K, 8 wwords] array
+    // output: words word0 .. word0 + wwords - 1 of every row, as a [K, 8 wwords]
+    // array; row k goes to row row_out[k] when a row order is given (the
+    // sorted rows of an act-order layer put back in their original order)
     const int64_t total = K * wwords;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
         const int64_t k = idx / wwords;
-        const int64_t j = word0 + (idx - k * wwords);
+        const int64_t jw = idx - k * wwords;
+        const int64_t j = word0 + jw;
+        int64_t dst = idx;
+        if (row_out) {
+            const int64_t r = __ldg(row_out + k);
+            if (r < 0 || r >= K) {
+                raise_status(status, kStatusBadIndex);
+                continue;
+            }
+            dst = r * wwords + jw;
+        }
         const int64_t gi = k / g;
         const uint32_t qw = __ldg(qweight + k * words + j);
         const uint32_t zw = __ldg(qzeros + gi * words + j);
@@ -34,7 +47,7 @@ dequant_kernel(const uint32_t *__restrict__ qweight, const uint32_t *__restrict_
         __half s[8], w[8];
         *reinterpret_cast<uint4 *>(s) = sraw;
         dequant_word(qw, zw, s, w);
-        *reinterpret_cast<uint4 *>(W + idx * 8) = *reinterpret_cast<const uint4 *>(w);
+        *reinterpret_cast<uint4 *>(W + dst * 8) = *reinterpret_cast<const uint4 *>(w);
     }
 }
 
@@ -101,7 +114,8 @@ cudaError_t launch_dequant_cols(const Problem &p, int64_t c0, int64_t nc, void *
     if (blocks < 1) return cudaSuccess;
     dequant_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
         reinterpret_cast<const uint32_t *>(p.qweight), reinterpret_cast<const uint32_t *>(p.qzeros),
-        static_cast<const __half *>(p.scales), static_cast<__half *>(W), p.K, words, p.g, c0 / 8, nc / 8);
+        static_cast<const __half *>(p.scales), static_cast<__half *>(W), p.K, words, p.g, c0 / 8, nc / 8,
+        p.row_perm, device_status_word());
     return cudaGetLastError();
 }
 

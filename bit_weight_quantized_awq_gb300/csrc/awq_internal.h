@@ -21,6 +21,8 @@ struct Problem {
     int64_t ldx = 0;        // elements between rows of x (0 = K): a K-slice of a wider x
     float *y32 = nullptr;   // if set: y32[M, N] += x . W in fp32 (no bias, no rounding),
                             // instead of writing y
+    const int32_t *row_perm = nullptr;   // dequantise-then-GEMM only: weight row k is
+                                         // row row_perm[k] of W (act-order layers)
 };
 
 // Per-(device, stream) scratch: fp32 split-K partials plus self-resetting
@@ -36,7 +38,7 @@ struct Scratch {
 // kStatusTimeout) for kernels to record device-side errors in.
 unsigned int *device_status_word();
 constexpr unsigned int kStatusTimeout = 1u;
-constexpr unsigned int kStatusBadIndex = 2u;   // a group index outside [0, G)
+constexpr unsigned int kStatusBadIndex = 2u;   // a group or row index out of range
 
 // Scratch for `stream` on the current device, grown to at least the given
 // sizes. Returns false if an allocation failed.
@@ -91,6 +93,12 @@ cudaError_t launch_gemm_f16(const Problem &p, const void *w16, cudaStream_t stre
 // kernels one prefill / GEMM-core launch enqueues on a GPU with `sms` SMs:
 // the persistent kernel, plus sk_fixup_kernel when a tile is split along k
 int prefill_launches(int64_t M, int64_t K, int64_t N, int sms);
+// act-order layers: rows of packed weights / columns of x in sorted order
+cudaError_t launch_gather_rows(const int32_t *src, const int32_t *perm, int32_t *dst, int64_t K,
+                               int64_t words, cudaStream_t stream);
+cudaError_t launch_gather_cols(const void *x, int64_t ldx, const int32_t *perm, void *xs, int64_t M,
+                               int64_t K, cudaStream_t stream);
+bool get_xs_scratch(cudaStream_t stream, size_t bytes, void **out);
 // fp16 weight columns per window of the dequantise-then-GEMM path
 int64_t dequant_gemm_window(int64_t K, int64_t N);
 

@@ -12,8 +12,9 @@ from __future__ import annotations
 
 import torch
 
-from ._binding import (AWQError, Path, Status, awq_dequant, awq_dequant_gidx, awq_linear_forward_gidx,
-                       awq_linear_forward_path, awq_pack, awq_quantize_rtn)
+from ._binding import (AWQError, Path, Status, awq_dequant, awq_dequant_gidx, awq_gidx_sort,
+                       awq_linear_forward_gidx, awq_linear_forward_path, awq_linear_forward_sorted, awq_pack,
+                       awq_permute_rows, awq_quantize_rtn)
 
 
 def _ptr(t):
@@ -130,6 +131,63 @@ def linear_forward_gidx(x: torch.Tensor, qweight: torch.Tensor, qzeros: torch.Te
                                  _ptr(bias), _ptr(out), M, K, N, G, _stream(dev))
     if st != Status.OK:
         raise AWQError(st, "awq_linear_forward_gidx")
+    return out.reshape(*x.shape[:-1], N)
+
+
+def gidx_sort(g_idx: torch.Tensor, groups: int) -> torch.Tensor:
+    """The row order that makes an act-order g_idx layer (every group holds
+    K / G rows) a grouped one: int32 [K] on the CPU, perm[i] = the original
+    row of sorted row i (awq_gidx_sort, a host routine of the library)."""
+    gi = g_idx.detach().to("cpu", torch.int32).contiguous()
+    K = gi.numel()
+    perm = torch.empty(K, dtype=torch.int32)
+    st = awq_gidx_sort(_ptr(gi), K, groups, _ptr(perm))
+    if st != Status.OK:
+        raise AWQError(st, "awq_gidx_sort")
+    return perm
+
+
+def prepare_act_order(qweight: torch.Tensor, g_idx: torch.Tensor, groups: int):
+    """(qweight_sorted, perm on the weights' device, group_size) for an
+    act-order layer: rows sorted by group once, on the GPU."""
+    dev = qweight.device
+    if dev.type != "cuda":
+        raise ValueError("the AWQ library runs on CUDA tensors only")
+    _check(qweight, "qweight", torch.int32, dev)
+    K, N = qweight.shape[0], qweight.shape[1] * 8
+    perm = gidx_sort(g_idx, groups).to(dev)
+    out = torch.empty_like(qweight)
+    st = awq_permute_rows(_ptr(qweight), _ptr(perm), _ptr(out), K, N, _stream(dev))
+    if st != Status.OK:
+        raise AWQError(st, "awq_permute_rows")
+    return out, perm, K // groups
+
+
+def linear_forward_sorted(x: torch.Tensor, perm: torch.Tensor, qweight_sorted: torch.Tensor,
+                          qzeros: torch.Tensor, scales: torch.Tensor, bias: torch.Tensor | None,
+                          group_size: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """The forward of an act-order layer prepared by prepare_act_order: x's
+    columns gathered in perm order, then the grouped forward."""
+    dev = qweight_sorted.device
+    if dev.type != "cuda":
+        raise ValueError("the AWQ library runs on CUDA tensors only")
+    for t, name, dt in ((x, "x", torch.float16), (perm, "perm", torch.int32),
+                        (qweight_sorted, "qweight_sorted", torch.int32), (qzeros, "qzeros", torch.int32),
+                        (scales, "scales", torch.float16)):
+        _check(t, name, dt, dev)
+    if bias is not None:
+        _check(bias, "bias", torch.float16, dev)
+    K, N = qweight_sorted.shape[0], qweight_sorted.shape[1] * 8
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=dev)
+    else:
+        _check(out, "out", torch.float16, dev)
+    st = awq_linear_forward_sorted(_ptr(x2), _ptr(perm), _ptr(qweight_sorted), _ptr(qzeros), _ptr(scales),
+                                   _ptr(bias), _ptr(out), M, K, N, group_size, _stream(dev))
+    if st != Status.OK:
+        raise AWQError(st, "awq_linear_forward_sorted")
     return out.reshape(*x.shape[:-1], N)
 
 

@@ -210,6 +210,40 @@ awq_status_t awq_linear_forward_gidx(const void *x, const int32_t *qweight, cons
                                      awq_stream_t stream);
 
 /*
+ * Act-order g_idx layers on the grouped kernels. When every group of a g_idx
+ * table holds the same number of rows g = K / G (the act-order tables of the
+ * GPTQ tuple the Linear Layer Factory page lists), sorting the rows by group
+ * turns the layer into an ordinary grouped one with group_size g and the same
+ * qzeros and scales; the forward then reads x's columns in that order:
+ *   y[m, n] = fp16_rn(sum_i x[m, perm[i]] * W[perm[i], n] + bias[n]),
+ * the g_idx forward's sum with its terms reordered.
+ *
+ * awq_gidx_sort -- HOST pointers, no CUDA call: perm[i] = the original row of
+ *   sorted row i, rows of each group in their original order (stable).
+ *   g_idx int32 [K] (read), perm int32 [K] (written). Returns
+ *   AWQ_ERR_INVALID_ARG unless K > 0, G > 0, K % G == 0, every entry lies in
+ *   [0, G) and every group holds exactly K / G rows.
+ * awq_permute_rows -- qweight_sorted[i, :] = qweight[perm[i], :], on the
+ *   device (once, when the layer is loaded). qweight, qweight_sorted int32
+ *   [K, N / 8], perm int32 [K]; N % 32 == 0. A perm entry outside [0, K)
+ *   writes a zero row and makes the next awq_last_device_status() return
+ *   AWQ_ERR_INVALID_ARG.
+ * awq_linear_forward_sorted -- the forward of such a layer: x's columns are
+ *   gathered in perm order into a per-(device, stream) scratch area of M x K
+ *   fp16 (allocated on first use), then awq_linear_forward runs on the sorted
+ *   weights with group_size = K / G. Arguments as awq_linear_forward, plus
+ *   perm (device, int32 [K]); K % 8 == 0. A perm entry outside [0, K) reads
+ *   as a zero activation and is reported as above.
+ */
+awq_status_t awq_gidx_sort(const int32_t *g_idx, int64_t K, int64_t G, int32_t *perm);
+awq_status_t awq_permute_rows(const int32_t *qweight, const int32_t *perm, int32_t *qweight_sorted,
+                              int64_t K, int64_t N, awq_stream_t stream);
+awq_status_t awq_linear_forward_sorted(const void *x, const int32_t *perm, const int32_t *qweight_sorted,
+                                       const int32_t *qzeros, const void *scales, const void *bias,
+                                       void *y, int64_t M, int64_t K, int64_t N, int64_t group_size,
+                                       awq_stream_t stream);
+
+/*
  * awq_pack -- packs 4-bit codes into the layer's int32 format, the inverse of
  * the unpacking every forward call does (I/O Contract of the WQLinear page:
  * eight 4-bit values per int32; the order is this library's reading):
