@@ -68,6 +68,31 @@ def test_quantize_ties_clamps_and_special_quotients(gpu):
         assert np.array_equal(got, ref), zval
 
 
+def test_quantize_exact_halves_and_their_neighbours_over_all_scale_exponents(gpu):
+    """Every half-integer quotient h in [-64.5, 64.5] for 512 scales spread
+    over all fp16 exponents (normal and subnormal), with W = h * s where that
+    is an fp16 value, and W one fp16 step above and below it: the quotients
+    the rounding decision is most sensitive to."""
+    rng = np.random.default_rng(12)
+    bits = rng.integers(1, 0x7C00, size=512).astype(np.uint16)    # positive finite, nonzero
+    svals = bits.view(np.float16)
+    halves = np.arange(-129, 130, 2) / 2.0                         # -64.5 .. 64.5
+    rows = []
+    for h in halves:
+        w = (h * svals.astype(np.float64)).astype(np.float16)
+        rows += [w, np.nextafter(w, np.float16(np.inf)), np.nextafter(w, np.float16(-np.inf))]
+    W = np.stack(rows).astype(np.float16)                          # [3 * 259, 512]
+    W[~np.isfinite(W)] = np.float16(0)
+    K, N = W.shape
+    s = np.tile(svals, (K, 1))
+    for zval in (0, 8):
+        qz = oracle.pack(np.full((K, N), zval, dtype=np.uint8))
+        ref = oracle.quantize_rtn(W, s, qz, 1)
+        got = quantize_rtn(torch.from_numpy(W).cuda(), torch.from_numpy(s).cuda(),
+                           torch.from_numpy(qz).cuda(), 1).cpu().numpy()
+        assert np.array_equal(got, ref), f"z={zval}: {(got != ref).sum()} words differ"
+
+
 @pytest.mark.parametrize("K,N,g", [(4096, 22016, 128), (11008, 4096, 128), (256, 64, -1)])
 def test_quantize_inverts_dequant(gpu, K, N, g):
     """awq_quantize_rtn(awq_dequant(q)) == q for the synthetic scales."""
