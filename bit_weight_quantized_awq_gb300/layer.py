@@ -41,24 +41,31 @@ def linear_forward(x: torch.Tensor, qweight: torch.Tensor, qzeros: torch.Tensor,
     dev = qweight.device
     if dev.type != "cuda":
         raise ValueError("the AWQ library runs on CUDA tensors only")
-    _check(x, "x", torch.float16, dev)
-    _check(qweight, "qweight", torch.int32, dev)
-    _check(qzeros, "qzeros", torch.int32, dev)
-    _check(scales, "scales", torch.float16, dev)
+    f16, i32 = torch.float16, torch.int32
+    # one combined test first (the common case), the detailed checks only to
+    # name what is wrong
+    if not (x.dtype == f16 and qweight.dtype == i32 and qzeros.dtype == i32 and scales.dtype == f16
+            and x.device == dev and qzeros.device == dev and scales.device == dev
+            and x.is_contiguous() and qweight.is_contiguous() and qzeros.is_contiguous()
+            and scales.is_contiguous()):
+        _check(x, "x", f16, dev)
+        _check(qweight, "qweight", i32, dev)
+        _check(qzeros, "qzeros", i32, dev)
+        _check(scales, "scales", f16, dev)
     if bias is not None:
-        _check(bias, "bias", torch.float16, dev)
+        _check(bias, "bias", f16, dev)
     K, N = qweight.shape[0], qweight.shape[1] * 8
     if x.shape[-1] != K:
         raise ValueError(f"x has {x.shape[-1]} input features, qweight has {K}")
     M = x.numel() // K
     if out is None:
-        out = torch.empty((M, N), dtype=torch.float16, device=dev)
+        out = torch.empty((M, N), dtype=f16, device=dev)
     else:
-        _check(out, "out", torch.float16, dev)
+        _check(out, "out", f16, dev)
         if out.numel() != M * N:
             raise ValueError("out has the wrong number of elements")
-    st = awq_linear_forward_path(_ptr(x), _ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(bias),
-                                 _ptr(out), M, K, N, group_size, _stream(dev), int(path))
+    st = awq_linear_forward_path(x.data_ptr(), qweight.data_ptr(), qzeros.data_ptr(), scales.data_ptr(),
+                                 _ptr(bias), out.data_ptr(), M, K, N, group_size, _stream(dev), int(path))
     if st != Status.OK:
         raise AWQError(st, "awq_linear_forward")
     return out.view(*x.shape[:-1], N)
