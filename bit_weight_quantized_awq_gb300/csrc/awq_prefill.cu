@@ -136,6 +136,7 @@ struct PrefillParams {
     int M, K, N, g;
     int64_t ldy;            // elements between rows of y (N, or more for a column window)
     int tiles_m, tiles_n, kiters;
+    int group_m;            // row blocks per band of the tile order (see tile_coords)
     int dp_waves;           // full waves of whole tiles, tile = cta + wave * gridDim.x
     int sk_tiles;           // tiles after those, split along k between sk_ctas CTAs
     int sk_ctas;
@@ -188,6 +189,21 @@ struct Segments {
         tile = p.dp_waves * gridDim.x + t;
     }
 };
+
+// Tile order: bands of group_m row blocks, the row block fastest inside a
+// band, then the column block. A wave of tiles then shares group_m blocks of
+// x and a run of weight column blocks, which stay in L2 while the wave runs;
+// with group_m = tiles_m this is plain row-fastest order.
+__host__ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int group_m,
+                                                     int &mi, int &ni)
+{
+    const int band = tile / (group_m * tiles_n);
+    const int first = band * group_m;
+    const int rows = tiles_m - first < group_m ? tiles_m - first : group_m;
+    const int r = tile - band * group_m * tiles_n;
+    mi = first + r % rows;
+    ni = r / rows;
+}
 
 __device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
     __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
@@ -302,8 +318,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             for (int si = 0; si < sg.count && ok; ++si) {
                 int tile, kb0, kb1;
                 sg.get(p, si, tile, kb0, kb1);
-                const int m0 = (tile % p.tiles_m) * BMT;
-                const int n0 = (tile / p.tiles_m) * BN;
+                int mi, ni;
+                tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mi, ni);
+                const int m0 = mi * BMT;
+                const int n0 = ni * BN;
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
                     if (!ptx::mbar_wait_bounded(ptx::smem_addr(tfree + s), ((it / kStages) & 1) ^ 1,
@@ -476,8 +494,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             sg.get(p, si, tile, kb0, kb1);
             const int ab0 = MH == 1 ? (acc_it & 1) : 0;
             const uint32_t full_parity = (uint32_t)((MH == 1 ? (acc_it >> 1) : acc_it) & 1);
-            const int m0 = (tile % p.tiles_m) * BMT;
-            const int n0 = (tile / p.tiles_m) * BN;
+            int mi, ni;
+            tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mi, ni);
+            const int m0 = mi * BMT;
+            const int n0 = ni * BN;
             const bool whole = kb0 == 0 && kb1 == p.kiters;
             // a piece of a stream-K tile goes to this CTA's slot: the first
             // piece of its range in slot 0, the last in slot 1
@@ -580,7 +600,7 @@ struct FixupParams {
     float *y32;
     int M, N;
     int64_t ldy;
-    int tiles_m, kiters;
+    int tiles_m, tiles_n, group_m, kiters;
     int first_tile;         // tile index of stream-K tile 0: dp_waves x the main grid's size
     int sk_tiles, sk_ctas;
 };
@@ -598,8 +618,10 @@ sk_fixup_kernel(const FixupParams p)
     const int cl = sk_cta_of(t * p.kiters + p.kiters - 1, units, p.sk_ctas);
     if (cl == cf) return;   // a single contributor took the whole tile and stored it
     const int tile = p.first_tile + t;
-    const int m = (tile % p.tiles_m) * (BM * MH) + h * BM + (int)threadIdx.x;
-    const int col0 = (tile / p.tiles_m) * BN + 32 * c;
+    int mi, ni;
+    tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mi, ni);
+    const int m = mi * (BM * MH) + h * BM + (int)threadIdx.x;
+    const int col0 = ni * BN + 32 * c;
     if (m >= p.M || col0 >= p.N) return;
     float acc[32];
 #pragma unroll
@@ -703,10 +725,27 @@ int group_rows_per_stage(int64_t g)
 // pieces of every tile that was split.
 struct Plan {
     int tiles_m, tiles_n, kiters;
+    int group_m;
     int dp_waves, sk_tiles, sk_ctas, ctas;
     bool split;             // some tile has more than one contributor
     bool ok;                // sizes within the kernel's index range
 };
+
+// Row blocks per band of the tile order. Whole waves in row-fastest order
+// sweep all of x once per wave. When x is larger than a share of L2, bands
+// of as many row blocks as fit that share are used instead, provided a band
+// still spans at least a wave of tiles: x is then read about once and the
+// weights once per band.
+constexpr int64_t kL2Share = 32ll << 20;
+
+int group_rows(int tiles_m, int tiles_n, int64_t K, int sms, int mh)
+{
+    const int64_t x_block = (int64_t)BM * mh * K * 2;      // one row block of x
+    if ((int64_t)tiles_m * x_block <= kL2Share) return tiles_m;
+    const int64_t gm = kL2Share / x_block;
+    if (gm < 1 || gm * tiles_n < sms) return tiles_m;
+    return (int)gm;
+}
 
 Plan plan_tiles(int64_t M, int64_t K, int64_t N, int sms, int mh)
 {
@@ -715,6 +754,7 @@ Plan plan_tiles(int64_t M, int64_t K, int64_t N, int sms, int mh)
     pl.tiles_m = (int)((M + BM * mh - 1) / (BM * mh));
     pl.tiles_n = (int)((N + BN - 1) / BN);
     pl.kiters = (int)((K + BK - 1) / BK);
+    pl.group_m = group_rows(pl.tiles_m, pl.tiles_n, K, sms, mh);
     const int64_t n_tiles = (int64_t)pl.tiles_m * pl.tiles_n;
     pl.dp_waves = (int)(n_tiles / sms);
     pl.sk_tiles = (int)(n_tiles - (int64_t)pl.dp_waves * sms);
@@ -795,6 +835,7 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int6
     p.M = M; p.K = K; p.N = N; p.g = g;
     p.ldy = ldy > 0 ? ldy : N;
     p.tiles_m = tiles_m; p.tiles_n = tiles_n; p.kiters = kiters;
+    p.group_m = pl.group_m;
     p.dp_waves = dp_waves; p.sk_tiles = sk_tiles; p.sk_ctas = sk_ctas;
     p.stage_tx = tx_bytes;
     const bool split = pl.split;
@@ -814,7 +855,7 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int6
     f.y = p.y;
     f.y32 = p.y32;
     f.M = M; f.N = N; f.ldy = p.ldy;
-    f.tiles_m = tiles_m; f.kiters = kiters;
+    f.tiles_m = tiles_m; f.tiles_n = tiles_n; f.group_m = pl.group_m; f.kiters = kiters;
     f.first_tile = dp_waves * ctas;
     f.sk_tiles = sk_tiles; f.sk_ctas = sk_ctas;
     cudaLaunchConfig_t cfg{};

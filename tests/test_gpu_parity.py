@@ -143,6 +143,14 @@ def test_prefill_stream_k(gpu, M, K, N, g, bias):
         assert torch.equal(run_path(pg, Path.PREFILL).view(torch.int16), y0.view(torch.int16))
 
 
+# x larger than the L2 share the tile order plans for: 18 row blocks of 256
+# in bands of 16 (the last band 2 rows high) times 10 column blocks, on the
+# fused kernel and on the GEMM core; sampled rows and column blocks.
+@pytest.mark.parametrize("path", [Path.PREFILL, Path.DEQUANT_GEMM])
+def test_banded_tile_order(gpu, path):
+    check_problem(make_problem(4608, 4096, 2560, 128, bias=True, seed=4608), paths=[path], full=False)
+
+
 # --------------------------------------------------------------------------
 # full-size workloads: sampled rows and column blocks
 # --------------------------------------------------------------------------
