@@ -61,10 +61,10 @@ NCU_TRAFFIC = {
     # 3 fused + sum, 3 dequant + GEMM + sum) over its 9 calls, every launch
     # measured from a cold L2
     "prefill-7b": {
-        "bytes_per_launch": 526029028,
+        "bytes_per_launch": 392143104,
         "sources": {
             "bit_weight_quantized_awq_gb300/csrc/awq_prefill.cu":
-                "b723f8238cf5bf1b904745808ff8d80e350ca5c77433384a8bf8e9bc15491070",
+                "b8d9f538a7341450feab58ff5cc632a6deb813447b161924640c15678fd5cf0b",
             "bit_weight_quantized_awq_gb300/csrc/awq_tcgen05.cuh":
                 "7583bdc482c3f999df48aafe74db217e2c2055ec6f41779622d85db462730d4a",
             "bit_weight_quantized_awq_gb300/csrc/awq_dequant.cu":
@@ -766,7 +766,9 @@ def run_shard_sweep(args, device, peaks):
     """Sharded layer on one GPU (the shards one after another): the 70B-class
     shapes split 2 or 4 ways by columns and by group-aligned rows, against
     the unsharded forward; weight GB/s or TFLOP/s of the whole sharded
-    forward, CUDA graph of back-to-back forwards over two weight copies."""
+    forward, CUDA graph of back-to-back forwards over two weight copies. At
+    M = 1 the column shards are timed twice: gathered in place (every shard
+    writing its slice of one output) and as separate outputs concatenated."""
     import bit_weight_quantized_awq_gb300 as awq
     from bit_weight_quantized_awq_gb300.shard import (column_parallel_forward, row_parallel_forward,
                                                       split_columns, split_rows)
@@ -786,12 +788,20 @@ def run_shard_sweep(args, device, peaks):
                 b = (torch.randn((N,), device=device, generator=gen) * 0.1).half()
                 copies.append((qw, qz, sc, b))
             x = torch.randn((M, K), device=device, generator=gen).half()
-            for mode, parts in (("unsharded", 1), ("columns", 2), ("columns", 4), ("rows", 2), ("rows", 4)):
+            modes = [("unsharded", 1), ("columns", 2), ("columns", 4), ("rows", 2), ("rows", 4)]
+            if M == 1:
+                # the single-token gather in place against separate outputs
+                # concatenated afterwards
+                modes[3:3] = [("columns_concat", 2), ("columns_concat", 4)]
+            for mode, parts in modes:
                 if mode == "unsharded":
                     fns = [lambda c=c: awq.linear_forward(x, c[0], c[1], c[2], c[3], g) for c in copies]
                 elif mode == "columns":
                     sh = [split_columns(c[0], c[1], c[2], c[3], parts) for c in copies]
                     fns = [lambda s=s: column_parallel_forward(x, s, g) for s in sh]
+                elif mode == "columns_concat":
+                    sh = [split_columns(c[0], c[1], c[2], c[3], parts) for c in copies]
+                    fns = [lambda s=s: torch.cat([awq.linear_forward(x, *t, g) for t in s], dim=-1) for s in sh]
                 else:
                     sh = [(split_rows(c[0], c[1], c[2], g, parts), c[3]) for c in copies]
                     fns = [lambda s=s: row_parallel_forward(x, s[0], s[1]) for s in sh]

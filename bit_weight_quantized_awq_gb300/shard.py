@@ -10,7 +10,9 @@ weights concatenated along out_features.
 Here the shards run one after another on one GPU:
 
 * ``split_columns`` / ``column_parallel_forward``: slices of N (whole packed
-  words); each slice is an ordinary forward, the outputs are concatenated.
+  words); each slice is an ordinary forward, the outputs are concatenated --
+  for a single token without a copy, every shard writing its slice of one
+  output (the page's single-token head path).
 * ``split_rows`` / ``row_parallel_forward``: group-aligned slices of K; every
   shard adds its fp32 product into one fp32 buffer from inside its kernel's
   epilogue (``awq_linear_forward_rows``, reading its slice of x in place),
@@ -96,9 +98,56 @@ def concat_columns(layers: list[tuple]) -> tuple:
     return qweight, qzeros, scales, bias
 
 
-def column_parallel_forward(x: torch.Tensor, shards: list[tuple], group_size: int) -> torch.Tensor:
-    """The forward of a column-sharded layer: each shard's output, concatenated."""
-    return torch.cat([linear_forward(x, qw, qz, sc, b, group_size) for (qw, qz, sc, b) in shards], dim=-1)
+def column_parallel_forward(x: torch.Tensor, shards: list[tuple], group_size: int,
+                            out: torch.Tensor | None = None) -> torch.Tensor:
+    """The forward of a column-sharded layer: the shards' outputs side by side,
+    shape (*x.shape[:-1], N) with N the shards' out_features added up. The
+    shards may differ in width (separate heads: Q, K, V, or a vocabulary cut
+    into unequal slices); each is (qweight, qzeros, scales, bias).
+
+    A single token (x holds one row): that row of y is contiguous, so each
+    shard's kernel writes its own slice of one output directly. The gathered
+    tensor is the only one allocated (none when ``out`` is given) and nothing
+    is copied afterwards. This is the single-token branch of the
+    vocabulary-sharded head on the Predibase Lorax "Tensor Parallel Layers"
+    page (TensorParallelHead, Description: for one-token batches the matmul
+    and the gather are fused so as to allocate less), applied to WQLinear
+    shards. With several rows a shard's part of y is strided, and the
+    shards' outputs are concatenated (the page's gather-then-concatenate
+    branch), into ``out`` when it is given.
+    """
+    if not shards:
+        raise ValueError("no shards")
+    K = shards[0][0].shape[0]
+    for (qw, _, _, _) in shards:
+        if qw.shape[0] != K:
+            raise ValueError("shards differ in in_features")
+    if x.shape[-1] != K:
+        raise ValueError(f"x has {x.shape[-1]} features, the shards hold {K}")
+    widths = [qw.shape[1] * 8 for (qw, _, _, _) in shards]
+    N = sum(widths)
+    M = x.numel() // K
+    dev = shards[0][0].device
+    if out is None:
+        if dev.type != "cuda":
+            raise ValueError("the AWQ library runs on CUDA tensors only")
+        out = torch.empty((M, N), dtype=torch.float16, device=dev)
+    else:
+        _check(out, "out", torch.float16, dev)
+        if out.numel() != M * N:
+            raise ValueError(f"out holds {out.numel()} elements, the gathered output {M * N}")
+    y = out.view(M, N)
+    if M == 1:
+        c0 = 0
+        for (qw, qz, sc, b), n in zip(shards, widths):
+            # a [1, n] slice of the row: contiguous, 16-byte aligned (c0 is a
+            # multiple of 8 halves)
+            linear_forward(x, qw, qz, sc, b, group_size, out=y[:, c0:c0 + n])
+            c0 += n
+    else:
+        torch.cat([linear_forward(x, qw, qz, sc, b, group_size).view(M, n)
+                   for (qw, qz, sc, b), n in zip(shards, widths)], dim=1, out=y)
+    return y.view(*x.shape[:-1], N)
 
 
 def row_parallel_forward(x: torch.Tensor, shards: list[tuple], bias: torch.Tensor | None,

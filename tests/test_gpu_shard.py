@@ -77,3 +77,57 @@ def test_fused_projection_equals_separate(gpu):
     ref = np.concatenate([oracle.forward(layers[0].x.numpy(), l.qweight.numpy(), l.qzeros.numpy(),
                                          l.scales.numpy(), l.bias.numpy(), 128) for l in layers], axis=1)
     assert_close(y, ref, "fused q/k/v")
+
+
+@pytest.mark.parametrize("widths,g", [((4096, 1024, 1024), 128), ((2048, 2048), -1), ((512, 8, 1024), 128)])
+def test_single_token_heads_gather_in_place(gpu, widths, g):
+    """One token over heads of unequal widths (the vocabulary-sharded head's
+    single-token branch): every shard writes its slice of one output. The
+    result is bit for bit the concatenation of the separate forwards (the
+    same kernels run on the same shapes), within tolerance of the oracle,
+    and with a caller's output nothing is allocated by torch."""
+    from bit_weight_quantized_awq_gb300 import linear_forward
+    K = 4096
+    heads = [make_problem(1, K, n, g, bias=(i != 1), seed=40 + i) for i, n in enumerate(widths)]
+    x = heads[0].x.cuda()
+    shards = [(h.qweight.cuda(), h.qzeros.cuda(), h.scales.cuda(), None if h.bias is None else h.bias.cuda())
+              for h in heads]
+    separate = torch.cat([linear_forward(x, *s, g) for s in shards], dim=-1)
+    out = torch.empty((1, sum(widths)), dtype=torch.float16, device="cuda")
+    column_parallel_forward(x, shards, g, out=out)   # library scratch set up before counting
+    torch.cuda.synchronize()
+    before = torch.cuda.memory_allocated()
+    y = column_parallel_forward(x, shards, g, out=out)
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == before
+    assert y.data_ptr() == out.data_ptr()
+    assert torch.equal(y.view(torch.int16), separate.view(torch.int16))
+    ref = np.concatenate([oracle.forward(heads[0].x.numpy(), h.qweight.numpy(), h.qzeros.numpy(), h.scales.numpy(),
+                                         None if h.bias is None else h.bias.numpy(), g) for h in heads], axis=1)
+    assert_close(y.cpu().numpy(), ref, f"single-token heads {widths}")
+
+
+def test_single_token_batch_shape_kept(gpu):
+    """x of shape [1, 1, K] (one token of a batch): the gathered output keeps
+    the leading dimensions."""
+    M, K, N, g = 1, 1024, 1024, 128
+    p = make_problem(M, K, N, g, bias=True, seed=50)
+    pg = p.to("cuda")
+    y = column_parallel_forward(pg.x.view(1, 1, K), split_columns(pg.qweight, pg.qzeros, pg.scales, pg.bias, 4), g)
+    assert y.shape == (1, 1, N)
+    assert_close(y.view(1, N).cpu().numpy(), oracle_reference(p), "single token, 3-D x")
+
+
+def test_multi_token_heads_into_callers_output(gpu):
+    """Several tokens: the shards' outputs are concatenated into the caller's
+    tensor, equal bit for bit to the unsharded column order."""
+    M, K, g = 12, 2048, 64
+    heads = [make_problem(M, K, n, g, bias=True, seed=60 + n) for n in (1024, 256)]
+    x = heads[0].x.cuda()
+    shards = [(h.qweight.cuda(), h.qzeros.cuda(), h.scales.cuda(), h.bias.cuda()) for h in heads]
+    out = torch.empty((M, 1280), dtype=torch.float16, device="cuda")
+    y = column_parallel_forward(x, shards, g, out=out)
+    assert y.data_ptr() == out.data_ptr()
+    from bit_weight_quantized_awq_gb300 import linear_forward
+    separate = torch.cat([linear_forward(x, *s, g) for s in shards], dim=-1)
+    assert torch.equal(y.view(torch.int16), separate.view(torch.int16))

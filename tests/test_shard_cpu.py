@@ -63,3 +63,23 @@ def test_split_rules():
         split_rows(p.qweight, p.qzeros, p.scales, 64, 3)
     shards = split_rows(p.qweight, p.qzeros, p.scales, 64, 4)
     assert [s[0].shape[0] for s in shards] == [64] * 4 and all(s[3] == 64 for s in shards)
+
+
+def test_column_parallel_forward_checks_shapes_before_any_launch():
+    """Host-side argument checks of the gathered column-parallel forward: they
+    raise before anything reaches the library (CPU tensors here)."""
+    import torch
+    from bit_weight_quantized_awq_gb300.shard import column_parallel_forward
+    a = make_problem(1, 256, 64, 64, seed=3)
+    b = make_problem(1, 128, 64, 64, seed=4)
+    sa = (a.qweight, a.qzeros, a.scales, None)
+    with pytest.raises(ValueError, match="no shards"):
+        column_parallel_forward(a.x, [], 64)
+    with pytest.raises(ValueError, match="in_features"):
+        column_parallel_forward(a.x, [sa, (b.qweight, b.qzeros, b.scales, None)], 64)
+    with pytest.raises(ValueError, match="features"):
+        column_parallel_forward(b.x, [sa], 64)
+    with pytest.raises(ValueError, match="CUDA"):
+        column_parallel_forward(a.x, [sa], 64)
+    with pytest.raises(ValueError):
+        column_parallel_forward(a.x, [sa], 64, out=torch.empty((1, 32), dtype=torch.float16))
