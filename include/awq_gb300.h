@@ -38,10 +38,14 @@
  *     word that awq_last_device_status() reads.
  *   - The library keeps, per (device, stream), a lazily created scratch area
  *     for split-K partial sums (allocated with cudaMalloc on first use on that
- *     stream, freed by awq_shutdown). Make the first call on a stream before
- *     capturing that stream into a CUDA graph.
- *   - Thread safety: calls may come from several host threads; calls on the
- *     same stream are ordered by the stream.
+ *     stream, freed by awq_shutdown). An area that has to grow for a larger
+ *     need (a prefill-sized call after decode-sized ones, say) is replaced
+ *     after a cudaStreamSynchronize of that stream, which a stream capture
+ *     does not allow: before capturing a stream into a CUDA graph, make on it
+ *     one call of every shape and path the graph will hold.
+ *   - Thread safety: calls may come from several host threads on different
+ *     streams. Two host threads must not call at the same time on one stream
+ *     (a growing scratch area could be freed under the other call).
  */
 #ifndef AWQ_GB300_H
 #define AWQ_GB300_H
