@@ -1,5 +1,8 @@
 """Torch-facing wrappers: allocate outputs, pass pointers and the current
-stream to the C ABI, reshape. No arithmetic happens here.
+stream to the C ABI, reshape. No arithmetic happens here. The library works
+on the current CUDA device, so the tensors must be on it (select it with
+``torch.cuda.set_device`` or ``torch.cuda.device`` when a process drives
+several GPUs).
 
 ``AWQLinear`` follows the WQLinear contract (Predibase Lorax "AWQ WQLinear"
 page): constructor arguments (w_bit, group_size, qweight, qzeros, scales,

@@ -32,6 +32,8 @@
  *   - All tensors are device pointers to row-major, contiguous arrays, and
  *     every base pointer must be 16-byte aligned (AWQ_ERR_MISALIGNED if not).
  *   - The caller owns every buffer; outputs are caller-allocated.
+ *   - Every call works on the current CUDA device (cudaSetDevice): its
+ *     pointers and `stream` must belong to that device.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
  *     Argument errors are returned before anything is enqueued. A device-side
  *     error (a bounded wait that timed out) is recorded in a per-device status
