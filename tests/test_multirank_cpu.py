@@ -65,3 +65,24 @@ def test_reference_arm_is_rank_zero_only(monkeypatch, capsys):
     monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--gpus", "2"])
     bench.main()
     assert called == [] and capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_on_one_rank(monkeypatch, capsys):
+    """At N = 1 the reference arm (the CPU oracle on a bounded sample) prints
+    one JSON line with the bench contract's keys, on the native arm's metric
+    and workload, and its cpu_baseline and e2e values equal to the line's."""
+    import json
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--steps", "3", "--warmup", "3"])
+    bench.main()
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
+    assert d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["unit"] == "weight GB/s"
+    assert d["config"]["workload"] == "decode-7b" and d["data"] == "synthetic"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
