@@ -39,6 +39,23 @@ MUTANTS = {
     "gidx_table_ignored": ("const int64_t row_group = g_idx[k];", "const int64_t row_group = k % G;"),
     "gidx_zero_of_wrong_row": ("int diff = (int)q[k * N + n] - (int)z[row_group * N + n];",
                                "int diff = (int)q[k * N + n] - (int)z[(k % G) * N + n];"),
+    "f16_encode_truncates": ("double s = round_half_even(ldexp(a, 10 - expo));",
+                             "double s = floor(ldexp(a, 10 - expo));"),
+    "f16_decode_subnormal_as_normal": ("v = ldexp((double)frac, -24);",
+                                       "v = ldexp((double)(1024 + frac), -25);"),
+    "f16_encode_subnormal_scale": ("double m = round_half_even(ldexp(a, 24));",
+                                   "double m = round_half_even(ldexp(a, 23));"),
+    "zero_point_of_group_zero": ("int d = (int)q[k * N + n] - (int)z[gi * N + n];",
+                                 "int d = (int)q[k * N + n] - (int)z[n];"),
+    "sum_rounded_to_f16_before_bias": ("j->y[r * N + j->n0 + n] = acc[n] + b;",
+                                       "j->y[r * N + j->n0 + n] = "
+                                       "awq_oracle_f16_to_f64(awq_oracle_f64_to_f16(acc[n])) + b;"),
+    "sampled_row_read_from_sample_index": ("double xv = awq_oracle_f16_to_f64(j->x[m * K + k]);",
+                                           "double xv = awq_oracle_f16_to_f64(j->x[r * K + k]);"),
+    "group_minus_one_rule_missing": ("int64_t g = (group_size == -1) ? in_features : group_size;",
+                                     "int64_t g = group_size;"),
+    "pack_keeps_high_bits": ("w |= (uint32_t)(codes[r * cols + 8 * j + i] & 0xFu) << (4 * i);",
+                             "w |= (uint32_t)codes[r * cols + 8 * j + i] << (4 * i);"),
 }
 
 
