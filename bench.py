@@ -1,28 +1,40 @@
 """Benchmark of the AWQ W4A16 linear forward on GB300.
 
-Metric: AWQ W4A16 GEMM throughput -- effective weight GB/s (packed weights +
-scales + zero points per call) and TFLOP/s -- with the fraction of the
-kernel's roofline.
+Metric: AWQ W4A16 GEMM throughput -- TFLOP/s and effective weight GB/s
+(packed weights + scales + zero points per call) -- over M from 1 to 8192,
+with the fraction of each kernel family's roofline.
 
-Default workload (one "step"): the decode GEMV set on 7B-class projection
-shapes, M in {1, 4, 16} x (K, N) in {(4096, 4096), (4096, 12288),
-(4096, 22016), (11008, 4096)}, group_size 128, no bias: 12 forward calls.
-Every (M, shape) call has its own weight copy (315 MB of distinct weights per
-step, more than twice the 129 MB L2), so each call reads its weights cold.
+Default workload (one "step", ``--workload full``): every measured
+configuration of the layer, 55 forward calls, group_size 128 unless stated:
+  * decode on 7B-class projection shapes: M in {1, 4, 16} x (K, N) in
+    {(4096, 4096), (4096, 12288), (4096, 22016), (11008, 4096)}, no bias;
+  * prefill on the 7B-class shapes: M in {512, 2048, 8192} x (K, N) in
+    {(4096, 12288), (4096, 22016), (11008, 4096)}, bias on M = 512 and 8192;
+  * full-row grouping: x [8, 256, 4096] (M = 2048), K = N = 4096,
+    group_size -1, with bias;
+  * the 70B-class M sweep: (K, N) in {(8192, 10240), (8192, 57344),
+    (28672, 8192)} x M in {1, 2, 4, 8, 16, 32, 64, 128, 512, 2048, 8192}.
+Every call has its own weight copy (4.9 GB of distinct weights per step, far
+more than the 129 MB L2), so each call reads its weights cold.
 
     python bench.py [--steps K] [--warmup W] [--impl native|reference]
+    python bench.py --workload decode-7b | prefill-7b | sweep-70b | fullrow-3d
     python bench.py --sweep --workload all    # per-problem table, every path
     python bench.py --sweep --workload quantize   # awq_quantize_rtn / awq_pack GB/s
     python bench.py --sweep --workload gidx       # g_idx forward: table and sorted (act-order) forms
     python bench.py --sweep --workload shard      # column/row-sharded layer on one GPU
 
-Timing: one CUDA graph per step (its launches each bracketed by external
-event-record nodes); the timed region replays K steps between a barrier +
-synchronize on both sides; per-launch kernel durations come from the event
-nodes of the last replays. Clocks are sampled with nvidia-smi during the
-timed region. Under torchrun every rank runs the same workload on its own GPU
-(replicas, weak scaling) and rank 0 prints one JSON line with the max time
-over ranks.
+Timing: the calls of a step are grouped by kernel family -- the decode
+kernel (HBM-bound) and the tcgen05 paths (tensor-bound) -- and each group is
+one CUDA graph of back-to-back launches. The timed region replays K steps
+between a barrier + synchronize on both sides, with a CUDA event on the
+launching stream before each group's graph and after the last, so every
+family's own time inside the timed region is measured, and with it its
+roofline fraction. Per-call times (``per_problem``) come from separate graphs
+with an event pair around every call, replayed after the timed region.
+Clocks are sampled with nvidia-smi during the timed region. Under torchrun
+every rank runs the same workload on its own GPU (replicas, weak scaling) and
+rank 0 prints one JSON line with the max time over ranks.
 """
 from __future__ import annotations
 
@@ -43,46 +55,19 @@ if ROOT not in sys.path:
 
 METRIC = "AWQ W4A16 GEMM TFLOP/s and weight GB/s vs M (1..8192), % of roofline, 1xGB300"
 
-# DRAM bytes per launch of the dominant kernel, from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum, mean over one step's
-# launches), valid only while the kernel sources hash to what was captured.
-NCU_TRAFFIC = {
-    "decode-7b": {
-        "bytes_per_launch": 26414571,
-        "sources": {
-            "bit_weight_quantized_awq_gb300/csrc/awq_decode.cu":
-                "e4079f348ce343b8b09f5e0ccba713ff09de901ebcbeeceacaf35185bc6ad29b",
-            "bit_weight_quantized_awq_gb300/csrc/awq_device.cuh":
-                "3b7d583fc00ea3a961fa897260e5f0245bcdd8b06cb38725fdece027d0787054",
-        },
-        "summary": "profiles/decode_kernel_decode-7b.md",
-    },
-    # per forward call: the bytes of one step's 21 launches (3 fused + sum,
-    # 3 fused + sum, 3 dequant + GEMM + sum) over its 9 calls, every launch
-    # measured from a cold L2
-    "prefill-7b": {
-        "bytes_per_launch": 392143104,
-        "sources": {
-            "bit_weight_quantized_awq_gb300/csrc/awq_prefill.cu":
-                "b8d9f538a7341450feab58ff5cc632a6deb813447b161924640c15678fd5cf0b",
-            "bit_weight_quantized_awq_gb300/csrc/awq_tcgen05.cuh":
-                "7583bdc482c3f999df48aafe74db217e2c2055ec6f41779622d85db462730d4a",
-            "bit_weight_quantized_awq_gb300/csrc/awq_dequant.cu":
-                "ab8c5a1fb918217b860b7c18914bc103a104ee75b046b6efa1498301bc0d4370",
-            "bit_weight_quantized_awq_gb300/csrc/awq_device.cuh":
-                "3b7d583fc00ea3a961fa897260e5f0245bcdd8b06cb38725fdece027d0787054",
-        },
-        "summary": "profiles/prefill_kernel_prefill-7b.md",
-    },
-}
+# DRAM bytes per launch of a kernel family, from one ncu capture of that
+# workload (dram__bytes_read.sum + dram__bytes_write.sum, mean over one step's
+# launches of the family), valid only while the kernel sources hash to what
+# was captured. Keys: (workload, family).
+NCU_TRAFFIC = {}
 
 
-def ncu_traffic(workload):
+def ncu_traffic(workload, family):
     """(bytes per launch, note) of the committed capture, or (None, why)."""
     import hashlib
-    rec = NCU_TRAFFIC.get(workload)
+    rec = NCU_TRAFFIC.get((workload, family))
     if rec is None:
-        return None, "no ncu capture of this workload"
+        return None, f"no ncu capture of the {family} family on this workload"
     root = os.path.dirname(os.path.abspath(__file__))
     for rel, digest in rec["sources"].items():
         try:
@@ -105,6 +90,9 @@ WORKLOADS = {
     "fullrow-3d": [(2048, 4096, 4096, -1, True)],
     "sweep-70b": [(M, K, N, 128, False) for (K, N) in SWEEP_SHAPES for M in SWEEP_M],
 }
+WORKLOADS["full"] = (WORKLOADS["decode-7b"] + WORKLOADS["prefill-7b"] + WORKLOADS["fullrow-3d"]
+                     + WORKLOADS["sweep-70b"])
+DEFAULT_WORKLOAD = "full"
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -297,11 +285,38 @@ def kernels_per_call(M, K, N, g, path_value: int) -> int:
     return n
 
 
+# kernel families of a step: the decode kernel (bound by HBM) and the tcgen05
+# paths -- the fused prefill kernel and the dequantise-then-GEMM path, whose
+# GEMM core is the same tensor-core pipeline (bound by the tensor cores)
+FAMILY_OF_PATH = {1: "generic", 2: "decode", 3: "tcgen05", 4: "tcgen05"}
+
+
+def call_paths(problems, path):
+    """The path every call takes (the library's automatic choice unless a
+    path is forced)."""
+    import bit_weight_quantized_awq_gb300 as awq
+    from bit_weight_quantized_awq_gb300 import Path
+    if path != Path.AUTO:
+        return [int(path)] * len(problems)
+    return [awq.awq_select_path(p[0], p[1], p[2], p[3]) for p in problems]
+
+
+def group_by_family(paths):
+    """[(family, [problem indices])], decode first, in problem order within each."""
+    order = ["decode", "generic", "tcgen05"]
+    fams = {}
+    for i, pth in enumerate(paths):
+        fams.setdefault(FAMILY_OF_PATH[pth], []).append(i)
+    return [(f, fams[f]) for f in order if f in fams]
+
+
 def run_native(args, problems, device):
     import bit_weight_quantized_awq_gb300 as awq
     from bit_weight_quantized_awq_gb300 import Path
     awq.load_library()
     path = Path[args.path.upper()]
+    paths = call_paths(problems, path)
+    fams = group_by_family(paths)
     sets = build_inputs(problems, device, 2 * L2_BYTES)
     stream = torch.cuda.Stream(device)
     handle = stream.cuda_stream
@@ -317,14 +332,16 @@ def run_native(args, problems, device):
     if st != 0:
         raise RuntimeError(awq.awq_status_string(st))
 
-    # timed graphs hold nothing but the launches, so that consecutive kernels
-    # may overlap as they would in a model (programmatic dependent launch);
-    # a second set with an event pair around every launch times each kernel
-    # on its own, after the timed region
-    graphs = [capture_step(items, path, stream, False) for items in sets]
+    # timed graphs hold nothing but the launches of one family, so that
+    # consecutive kernels may overlap as they would in a model (programmatic
+    # dependent launch); a second set with an event pair around every launch
+    # times each call on its own, after the timed region
+    graphs = [[capture_step([items[i] for i in idx], path, stream, False)[0] for (_, idx) in fams]
+              for items in sets]
     use_events = True
     try:
-        ev_graphs = [capture_step(items, path, stream, True) for items in sets]
+        ev_graphs = [[capture_step([items[i] for i in idx], path, stream, True) for (_, idx) in fams]
+                     for items in sets]
     except Exception:
         use_events = False
         ev_graphs = []
@@ -332,23 +349,28 @@ def run_native(args, problems, device):
     # the stream the timing events are recorded on
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            graphs[i % len(graphs)][0].replay()
+            for g in graphs[i % len(graphs)]:
+                g.replay()
     torch.cuda.synchronize(device)
 
+    nf = len(fams)
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nf + 1)] for _ in range(args.steps)]
     ws, rank, local = dist_env()
     barrier(device)
     with ClockSampler(torch.cuda.current_device() if ws == 1 else local) as clk:
         barrier(device)
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
-            start.record(stream)
             for i in range(args.steps):
-                graphs[i % len(graphs)][0].replay()
-            end.record(stream)
+                for f, g in enumerate(graphs[i % len(graphs)]):
+                    marks[i][f].record(stream)
+                    g.replay()
+                marks[i][nf].record(stream)
         barrier(device)
-    elapsed = start.elapsed_time(end) / 1e3
     clocks = clk.summary()
+    elapsed = marks[0][0].elapsed_time(marks[-1][nf]) / 1e3
+    # each family's own time inside the timed region (summed over the steps)
+    fam_s = [sum(marks[i][f].elapsed_time(marks[i][f + 1]) for i in range(args.steps)) / 1e3
+             for f in range(nf)]
 
     st = awq.awq_last_device_status(handle)
     if st != 0:
@@ -359,27 +381,30 @@ def run_native(args, problems, device):
     abytes = sum(algo_bytes(*p) for p in problems)
     max_el, tot_wbytes = aggregate_ranks(elapsed, wbytes * args.steps, device)
     _, tot_flops = aggregate_ranks(elapsed, fl * args.steps, device)
+    fam_max = [aggregate_ranks(t, 0.0, device)[0] for t in fam_s]
 
     per_problem = None
     if use_events:
         per_problem = [[] for _ in problems]
         with torch.cuda.stream(stream):
             for rep in range(3):
-                for (g, _) in ev_graphs:
-                    g.replay()
+                for gs in ev_graphs:
+                    for (g, _) in gs:
+                        g.replay()
                 stream.synchronize()
                 if rep == 0:
                     continue   # warm-up pass
-                for (_, evs) in ev_graphs:
-                    for j, (e0, e1) in enumerate(evs):
-                        per_problem[j].append(e0.elapsed_time(e1) / 1e3)
+                for gs in ev_graphs:
+                    for (_, evs), (_, idx) in zip(gs, fams):
+                        for j, (e0, e1) in zip(idx, evs):
+                            per_problem[j].append(e0.elapsed_time(e1) / 1e3)
+    launches_per_call = [kernels_per_call(p[0], p[1], p[2], p[3], pth) for p, pth in zip(problems, paths)]
     return {"elapsed": max_el, "tot_wbytes": tot_wbytes, "tot_flops": tot_flops,
             "wbytes": wbytes, "flops": fl, "abytes": abytes, "clocks": clocks,
             "per_problem": per_problem, "copies": len(sets), "graph_events": use_events,
-            "launches": args.steps * sum(
-                kernels_per_call(p[0], p[1], p[2], p[3],
-                                 int(path) if path != Path.AUTO else awq.awq_select_path(p[0], p[1], p[2], p[3]))
-                for p in problems),
+            "paths": paths, "families": fams, "family_s": fam_max,
+            "launches_per_call": launches_per_call,
+            "launches": args.steps * sum(launches_per_call),
             "sets": sets}
 
 
@@ -455,7 +480,7 @@ def oracle_inputs(problems, cache, idx, col_words=None):
 def oracle_step(problems, cache, col_words=None, which=None, max_rows=None):
     """The oracle on the problems (all of them, or only index `which`), over
     all columns or the first `col_words` packed words, and all rows or the
-    first `max_rows`. Returns the weight bytes it processed."""
+    first `max_rows`. Returns the flops it performed (2 x rows x K x columns)."""
     import numpy as np
     import oracle
     done = 0
@@ -464,8 +489,27 @@ def oracle_step(problems, cache, col_words=None, which=None, max_rows=None):
         x, qws, qzs, scs, bs = oracle_inputs(problems, cache, idx, col_words)
         rows = None if max_rows is None or max_rows >= M else np.arange(max_rows, dtype=np.int64)
         oracle.forward(x, qws, qzs, scs, bs, g, rows=rows)
-        done += weight_bytes(K, qws.shape[1] * 8, g)
+        done += 2 * (M if rows is None else len(rows)) * K * qws.shape[1] * 8
     return done
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 # fp64 multiply-adds above which a whole step is too slow for the host cores
@@ -476,7 +520,7 @@ CPU_SAMPLE_COL_FRACTION = 8
 
 def cpu_baseline(problems, budget_s=12.0):
     """The oracle on whole steps of the workload (every problem, every row and
-    column), repeated until about `budget_s` has passed; weight GB/s. When a
+    column), repeated until about `budget_s` has passed; TFLOP/s. When a
     whole step holds more than CPU_FULL_STEP_MACS multiply-adds (the prefill
     workloads: hours of fp64 work), every problem runs on its first
     CPU_SAMPLE_ROWS rows and the first 1/CPU_SAMPLE_COL_FRACTION of its
@@ -487,6 +531,7 @@ def cpu_baseline(problems, budget_s=12.0):
     cache = {}
     oracle_step(problems, cache, col_words=1)   # input generation stays outside the timing
     macs = sum(M * K * N for (M, K, N, _, _) in problems)
+    cores, model = os.cpu_count(), cpu_model()
     if macs <= CPU_FULL_STEP_MACS:
         t0 = time.perf_counter()
         done, steps = 0, 0
@@ -496,10 +541,10 @@ def cpu_baseline(problems, budget_s=12.0):
             if time.perf_counter() - t0 > budget_s:
                 break
         el = time.perf_counter() - t0
-        return {"value": done / el / 1e9, "unit": "weight GB/s", "cores": os.cpu_count(),
+        return {"value": done / el / 1e12, "unit": "TFLOP/s", "cores": cores, "cpu_model": model,
                 "kind": "oracle",
                 "sample": f"{steps} full step(s) of the workload ({len(problems)} problems, all rows "
-                          f"and columns), fp64 oracle on {os.cpu_count()} threads, {el:.1f} s"}
+                          f"and columns), fp64 oracle on {cores} threads ({model}), {el:.1f} s"}
     # T(rows) = T_dequant + rows * T_row: the oracle dequantises W16 once per
     # call, then spends the same time on every row. Both parts are timed.
     import oracle as orc
@@ -518,47 +563,57 @@ def cpu_baseline(problems, budget_s=12.0):
             t_r = time.perf_counter() - t0
             per_row = max(t_r - t_deq, 0.0) / r
             full_s += (t_deq + M * per_row) * (N // 8) / words
-            done += weight_bytes(K, N, g)
+            done += flops(M, K, N)
         passes += 1
         if time.perf_counter() - t_start > budget_s:
             break
     el = time.perf_counter() - t_start
-    return {"value": done / full_s / 1e9, "unit": "weight GB/s", "cores": os.cpu_count(),
+    return {"value": done / full_s / 1e12, "unit": "TFLOP/s", "cores": cores, "cpu_model": model,
             "kind": "oracle",
             "sample": f"{passes} pass(es) over the {len(problems)} problems, each on its first "
                       f"{CPU_SAMPLE_ROWS} rows and first 1/{CPU_SAMPLE_COL_FRACTION} of the columns; "
                       f"a whole call extrapolated as (T_dequant + M x (T_rows - T_dequant) / rows) "
-                      f"x columns / sampled columns, with the oracle's dequant timed alone; fp64 oracle on {os.cpu_count()} threads, {el:.1f} s"}
+                      f"x columns / sampled columns, with the oracle's dequant timed alone; fp64 oracle "
+                      f"on {cores} threads ({model}), {el:.1f} s"}
+
+
+REF_SAMPLE_WORDS = 8      # first 64 output columns
+REF_SAMPLE_ROWS = 64      # first 64 rows
 
 
 def run_reference(args, problems):
     """--impl reference: the oracle on this workload, timed on the host
-    cores. Each step is one problem (in rotation) over its first 8 packed
-    words (64 output columns), so that K + W steps end within minutes."""
+    cores. Each step is one problem (in rotation) over its first 64 rows and
+    its first 8 packed words (64 output columns), so that K + W steps end
+    within minutes; TFLOP/s of the work done."""
     import oracle
     oracle.build()
     cache = {}
-    for i in range(len(problems)):
-        oracle_step(problems, cache, col_words=8, which=i)
+    kw = dict(col_words=REF_SAMPLE_WORDS, max_rows=REF_SAMPLE_ROWS)
+    # inputs of the problems the steps will use, generated outside the timing
+    for i in sorted({i % len(problems) for i in range(max(args.steps, args.warmup))}):
+        oracle_step(problems, cache, which=i, **kw)
     for i in range(args.warmup):
-        oracle_step(problems, cache, col_words=8, which=i % len(problems))
+        oracle_step(problems, cache, which=i % len(problems), **kw)
     t0 = time.perf_counter()
     done = 0
     for i in range(args.steps):
-        done += oracle_step(problems, cache, col_words=8, which=i % len(problems))
+        done += oracle_step(problems, cache, which=i % len(problems), **kw)
     el = time.perf_counter() - t0
-    value = done / el / 1e9
-    sample = (f"each step: one of the {len(problems)} problems in rotation, all rows, first 64 "
-              f"output columns; fp64 oracle on {os.cpu_count()} threads")
+    value = done / el / 1e12
+    cores, model = os.cpu_count(), cpu_model()
+    sample = (f"each step: one of the {len(problems)} problems in rotation, its first {REF_SAMPLE_ROWS} "
+              f"rows and first {8 * REF_SAMPLE_WORDS} output columns; fp64 oracle on {cores} threads "
+              f"({model})")
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "weight GB/s",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "problems": len(problems)},
-        "cpu_baseline": {"value": value, "unit": "weight GB/s", "cores": os.cpu_count(),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "cpu_model": model,
                          "kind": "oracle", "sample": sample},
-        "e2e": {"value": value, "unit": "weight GB/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -845,14 +900,15 @@ def main():
     ap = argparse.ArgumentParser(description=__doc__,
                                  formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", default="decode-7b", choices=list(WORKLOADS) + ["all", "quantize", "gidx", "shard"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=list(WORKLOADS) + ["all", "quantize", "gidx", "shard"])
     ap.add_argument("--path", default="auto", choices=["auto", "generic", "decode", "prefill", "dequant_gemm"])
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-out", default=None)
-    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--e2e-steps", type=int, default=0, help="0: about one second of steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -861,7 +917,7 @@ def main():
     ws, rank, local = dist_env()
     if args.impl == "reference":
         if rank == 0:
-            run_reference(args, WORKLOADS[args.workload if args.workload != "all" else "decode-7b"])
+            run_reference(args, WORKLOADS[args.workload if args.workload in WORKLOADS else DEFAULT_WORKLOAD])
         return
 
     if ws > 1:
@@ -886,54 +942,30 @@ def main():
 
     problems = WORKLOADS[args.workload]
     r = run_native(args, problems, device)
-    e2e_el, h2d, d2h = run_e2e(args, problems, device, r["sets"], args.e2e_steps)
-    e2e_el, e2e_units = aggregate_ranks(e2e_el, r["wbytes"] * args.e2e_steps, device)
+    step_s = r["elapsed"] / args.steps
+    e2e_steps = args.e2e_steps if args.e2e_steps else max(3, min(200, int(1.0 / max(step_s, 1e-6))))
+    e2e_el, h2d, d2h = run_e2e(args, problems, device, r["sets"], e2e_steps)
+    e2e_el, e2e_units = aggregate_ranks(e2e_el, r["flops"] * e2e_steps, device)
 
-    import bit_weight_quantized_awq_gb300 as awq
-    paths = [awq.awq_select_path(p[0], p[1], p[2], p[3]) for p in problems]
-    roof, per = None, None
-    names = {1: "generic_forward_kernel", 2: "decode_kernel", 3: "prefill_kernel",
-             4: "prefill_kernel (GEMM core on dequant_kernel windows)"}
-    dominant = max(set(paths), key=paths.count)
-    # the fused prefill kernel and the dequantise-then-GEMM path both run the
-    # tcgen05 contraction: one tensor-bound family
-    family = lambda pth: 3 if pth in (3, 4) else pth
-    if all(family(pth) == family(dominant) for pth in paths):
-        # every launch of the step is the dominant kernel: its average launch
-        # duration is the timed region over the launches in it
-        launch_s = r["elapsed"] / (args.steps * len(problems))
-        achieved = r["abytes"] / len(problems) / launch_s / 1e9
-        traffic, traffic_note = ncu_traffic(args.workload)
-        if dominant in (3, 4):
-            # the tcgen05 contraction: fp16 operands, whose nominal dense rate
-            # equals bf16's, so the measured bf16 cuBLAS peak is the roof
-            tf = r["flops"] / len(problems) / launch_s / 1e12
-            roof = {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": tf / peaks["bf16_tflops"], "traffic": traffic, "traffic_source": traffic_note,
-                    "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json bf16_tflops, burst; fp16 = bf16 nominal)",
-                    "kernel": names.get(dominant, "?"),
-                    "flops_per_launch_avg": r["flops"] / len(problems),
-                    "launch_us_avg": launch_s * 1e6,
-                    "how": "algorithmic flops per forward call / (timed region / calls), back-to-back "
-                           "graph replays; a call on the dequantise-then-GEMM path is its dequant_kernel "
-                           "launch and its GEMM launch"}
-        else:
-            roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "traffic_source": traffic_note,
-                    "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
-                    "kernel": names.get(dominant, "?"),
-                    "bytes_per_launch_avg": r["abytes"] / len(problems),
-                    "launch_us_avg": launch_s * 1e6,
-                    "how": "algorithmic bytes per launch / (timed region / launches), back-to-back graph replays"}
+    paths = r["paths"]
+    rooflines = family_rooflines(r, problems, args, peaks)
+    # the roofline of the family that takes most of the step's time
+    roof = max(rooflines, key=lambda x: x["share_of_step"]) if rooflines else None
+    per = None
     if r["per_problem"]:
-        avg = [statistics.mean(ts) for ts in r["per_problem"]]
-        per = [{"M": p[0], "K": p[1], "N": p[2], "us_isolated": round(a * 1e6, 3),
-                "hbm_frac_isolated": round(algo_bytes(*p) / a / 1e9 / peaks["hbm_gbs"], 4),
-                "weight_gbs_isolated": round(weight_bytes(p[1], p[2], p[3]) / a / 1e9, 1)}
-               for p, a in zip(problems, avg)]
+        per = []
+        for p, pth, ts in zip(problems, paths, r["per_problem"]):
+            a_s = statistics.mean(ts)
+            per.append({"M": p[0], "K": p[1], "N": p[2], "g": p[3], "bias": p[4],
+                        "path": FAMILY_OF_PATH.get(pth, "?") if pth != 4 else "dequant_gemm",
+                        "us_isolated": round(a_s * 1e6, 3),
+                        "tflops": round(flops(p[0], p[1], p[2]) / a_s / 1e12, 2),
+                        "weight_gbs": round(weight_bytes(p[1], p[2], p[3]) / a_s / 1e9, 1),
+                        "hbm_frac": round(algo_bytes(*p) / a_s / 1e9 / peaks["hbm_gbs"], 4),
+                        "tc_frac": round(flops(p[0], p[1], p[2]) / a_s / 1e12 / peaks["bf16_tflops"], 4)})
 
     line = {
-        "metric": METRIC, "value": r["tot_wbytes"] / r["elapsed"] / 1e9, "unit": "weight GB/s",
+        "metric": METRIC, "value": r["tot_flops"] / r["elapsed"] / 1e12, "unit": "TFLOP/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": r["elapsed"] / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16",
@@ -944,14 +976,18 @@ def main():
                    "l2": f"inputs larger than L2: {r['copies']} weight copies, "
                          f"{r['wbytes'] * r['copies'] / 2**20:.0f} MiB of distinct weights",
                    "parallelism": f"replicas x{ws}",
-                   "timing": "CUDA graph per step replayed back to back, CUDA events around the "
-                             "timed region; per_problem: separate graphs with an event pair per launch"},
-        "tflops": r["tot_flops"] / r["elapsed"] / 1e12,
+                   "timing": "one CUDA graph per kernel family per step, replayed back to back; CUDA "
+                             "events on the launching stream around every family's graph in the timed "
+                             "region; per_problem: separate graphs with an event pair per call, replayed "
+                             "after the timed region"},
+        "weight_gbs": r["tot_wbytes"] / r["elapsed"] / 1e9,
         "roofline": roof,
+        "rooflines": rooflines,
         "per_problem": per,
-        "e2e": {"value": e2e_units / e2e_el / 1e9, "unit": "weight GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "api": "bit_weight_quantized_awq_gb300.linear_forward, eager; per step one pinned host-to-device copy of all x and one device-to-host copy of all y"},
+        "e2e": {"value": e2e_units / e2e_el / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "api": "bit_weight_quantized_awq_gb300.linear_forward, eager; per step one pinned "
+                       "host-to-device copy of all x and one device-to-host copy of all y"},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
@@ -962,6 +998,53 @@ def main():
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def family_rooflines(r, problems, args, peaks):
+    """One roofline block per kernel family of the step, from that family's
+    own time inside the timed region: the decode kernel against the measured
+    HBM copy bandwidth (algorithmic bytes per launch / average launch
+    duration; one launch per decode call), the tcgen05 paths against the
+    measured dense bf16 peak (fp16's nominal rate equals bf16's; algorithmic
+    flops per call / average call duration, a call being the fused prefill
+    kernel or the dequant + GEMM-core pair, with the stream-K sum kernel
+    where a tile is split)."""
+    out = []
+    total = sum(r["family_s"])
+    for (fam, idx), t in zip(r["families"], r["family_s"]):
+        calls = len(idx) * args.steps
+        launches = sum(r["launches_per_call"][i] for i in idx) * args.steps
+        traffic, traffic_note = ncu_traffic(args.workload, fam)
+        if fam == "decode":
+            nbytes = sum(algo_bytes(*problems[i]) for i in idx) * args.steps
+            launch_s = t / launches
+            achieved = nbytes / launches / launch_s / 1e9
+            out.append({"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                        "traffic_source": traffic_note,
+                        "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
+                        "kernel": "decode_kernel", "calls_per_step": len(idx),
+                        "bytes_per_launch_avg": nbytes / launches, "launch_us_avg": launch_s * 1e6,
+                        "share_of_step": t / total,
+                        "how": "algorithmic bytes (packed weights + scales + zero points + x + y) per "
+                               "launch / (the family's time in the timed region / its launches)"})
+        elif fam == "tcgen05":
+            fl = sum(flops(*problems[i][:3]) for i in idx) * args.steps
+            call_s = t / calls
+            tf = fl / calls / call_s / 1e12
+            out.append({"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                        "frac": tf / peaks["bf16_tflops"],
+                        "frac_of_sustained": tf / peaks["bf16_tflops_sustained"],
+                        "traffic": traffic, "traffic_source": traffic_note,
+                        "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json bf16_tflops, burst; "
+                                       "fp16 = bf16 nominal)",
+                        "kernel": "prefill_kernel (fused, or GEMM core after dequant_kernel)",
+                        "calls_per_step": len(idx), "launches_per_step": launches // args.steps,
+                        "flops_per_call_avg": fl / calls, "call_us_avg": call_s * 1e6,
+                        "share_of_step": t / total,
+                        "how": "algorithmic flops per call / (the family's time in the timed region / "
+                               "its calls)"})
+    return out
 
 
 if __name__ == "__main__":

@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     AWQError,
     Path,
     Status,
+    awq_decode_tile_columns,
     awq_dequant,
     awq_dequant_gidx,
     awq_gemm_f16,

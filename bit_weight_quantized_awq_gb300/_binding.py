@@ -22,6 +22,7 @@ EXPORTED = (
     "awq_path_supported",
     "awq_select_path",
     "awq_forward_launches",
+    "awq_decode_tile_columns",
     "awq_dequant",
     "awq_status_string",
     "awq_last_device_status",
@@ -94,6 +95,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.awq_select_path.restype = _INT
         lib.awq_forward_launches.argtypes = [_I64, _I64, _I64, _I64, _INT]
         lib.awq_forward_launches.restype = _INT
+        lib.awq_decode_tile_columns.argtypes = [_I64, _I64, _I64, _I64]
+        lib.awq_decode_tile_columns.restype = _INT
         lib.awq_dequant.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P]
         lib.awq_dequant.restype = _INT
         lib.awq_status_string.argtypes = [_INT]
@@ -151,6 +154,10 @@ def awq_select_path(M, K, N, group_size) -> int:
 
 def awq_forward_launches(M, K, N, group_size, path=0) -> int:
     return load_library().awq_forward_launches(M, K, N, group_size, int(path))
+
+
+def awq_decode_tile_columns(M, K, N, group_size) -> int:
+    return load_library().awq_decode_tile_columns(M, K, N, group_size)
 
 
 def awq_dequant(qweight, qzeros, scales, W, K, N, group_size, stream) -> int:

@@ -6,6 +6,7 @@
 // the ABI has no other width), out_features = 8 x qweight columns so
 // N % 8 == 0, group_size -1 means K, and K % group_size == 0. Where the page
 // asserts, this layer returns a status instead; nothing aborts.
+#include <atomic>
 #include <cstdint>
 #include <map>
 #include <mutex>
@@ -28,7 +29,8 @@ __device__ unsigned int g_device_status = 0;
 namespace {
 
 std::mutex g_mutex;
-std::map<int, unsigned int *> g_status_addr;                  // device -> &g_device_status
+// device -> (&g_device_status on it, cache generation it was looked up in)
+std::map<int, std::pair<unsigned int *, unsigned>> g_status_addr;
 
 struct ScratchEntry {
     float *partials = nullptr;
@@ -48,12 +50,13 @@ unsigned int *device_status_word()
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    const unsigned gen = cache_generation();
     std::lock_guard<std::mutex> lock(g_mutex);
     auto it = g_status_addr.find(dev);
-    if (it != g_status_addr.end()) return it->second;
+    if (it != g_status_addr.end() && it->second.second == gen) return it->second.first;
     void *addr = nullptr;
     if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return nullptr;
-    g_status_addr[dev] = static_cast<unsigned int *>(addr);
+    g_status_addr[dev] = std::make_pair(static_cast<unsigned int *>(addr), gen);
     return static_cast<unsigned int *>(addr);
 }
 
@@ -142,18 +145,27 @@ bool get_xs_scratch(cudaStream_t stream, size_t bytes, void **out)
     return grow_area(stream, bytes, &ScratchEntry::xs, &ScratchEntry::xs_bytes, out);
 }
 
-// Drops the counters of every scratch area on this device so that the next
-// call re-zeroes them (used after a device-side timeout left some non-zero).
-static void reset_scratch_counters(int dev)
+// Zeroes, in place, the split-K arrival counters of every scratch area on
+// this device (a kernel whose bounded wait ran out leaves some non-zero). The
+// caller has synchronised the device, so no queued kernel still uses them.
+// The allocations stay where they are: CUDA graphs captured earlier hold
+// these pointers and remain valid.
+static cudaError_t reset_scratch_counters(int dev)
 {
     std::lock_guard<std::mutex> lock(g_mutex);
+    cudaError_t first = cudaSuccess;
     for (auto &kv : g_scratch) {
-        if (kv.first.first != dev) continue;
-        if (kv.second.counters) cudaFree(kv.second.counters);
-        kv.second.counters = nullptr;
-        kv.second.n_counters = 0;
+        if (kv.first.first != dev || !kv.second.counters) continue;
+        const cudaError_t e = cudaMemset(kv.second.counters, 0, kv.second.n_counters * sizeof(unsigned int));
+        if (first == cudaSuccess) first = e;
     }
+    const cudaError_t e = cudaDeviceSynchronize();
+    return first != cudaSuccess ? first : e;
 }
+
+std::atomic<unsigned> g_cache_generation{1};
+
+unsigned cache_generation() { return g_cache_generation.load(std::memory_order_acquire); }
 
 } // namespace awq
 
@@ -243,6 +255,13 @@ int awq_select_path(int64_t M, int64_t K, int64_t N, int64_t group_size)
     Problem p{};
     p.M = M; p.K = K; p.N = N; p.g = g; p.G = K / g;
     return (int)auto_path(p);
+}
+
+int awq_decode_tile_columns(int64_t M, int64_t K, int64_t N, int64_t group_size)
+{
+    int64_t g = 0;
+    if (M < 0 || check_shape(K, N, group_size, &g) != AWQ_OK) return -1;
+    return awq::decode_tile_columns(M, K, N, g);
 }
 
 int awq_forward_launches(int64_t M, int64_t K, int64_t N, int64_t group_size, awq_path_t path)
@@ -512,9 +531,12 @@ awq_status_t awq_last_device_status(awq_stream_t stream)
     if (cudaMemcpy(addr, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
         return AWQ_ERR_CUDA;
     if (word & awq::kStatusTimeout) {
+        // the kernel that gave up may have run on any stream of this device:
+        // wait for all of them, then zero every stream's counters in place
         int dev = 0;
-        cudaGetDevice(&dev);
-        awq::reset_scratch_counters(dev);
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
+            awq::reset_scratch_counters(dev) != cudaSuccess)
+            return AWQ_ERR_CUDA;
         return AWQ_ERR_TIMEOUT;
     }
     if (word & awq::kStatusBadIndex) return AWQ_ERR_INVALID_ARG;
@@ -534,6 +556,11 @@ void awq_shutdown(void)
         if (kv.second.xs) cudaFree(kv.second.xs);
     }
     awq::g_scratch.clear();
+    awq::g_status_addr.clear();
+    // per-device lookups cached by the kernel launchers (symbol addresses,
+    // function attributes) are redone on the next call: after a
+    // cudaDeviceReset they would be stale
+    awq::g_cache_generation.fetch_add(1, std::memory_order_acq_rel);
     cudaSetDevice(prev);
 }
 

@@ -9,7 +9,7 @@
 //
 //  * Work: the K x N weight matrix is cut into column tiles of CW 128-byte
 //    chunks of packed words (CW = 1: 256 columns; CW = 2: 512 columns, used
-//    when N is a multiple of 512 and at least 8192) and stages of 32 KB of
+//    when N is a multiple of 512 and at least 32768) and stages of 32 KB of
 //    packed weights (256 / CW k-rows). The (tile, stage) iterations,
 //    tile-major, are split evenly between the CTAs (one per SM): each CTA
 //    streams a contiguous run of them ("stream-K"). Rows 256 bytes wide keep
@@ -24,8 +24,8 @@
 //    each stage thread 0 refills the slot released one stage earlier, so it
 //    seldom waits. Issuing a TMA instruction costs on the order of a hundred
 //    cycles, so each one moves as many bytes as the box limits allow.
-//  * Math: 16 warps, each taking 64 rows x 64 columns of every stage (four
-//    16-row chunks): 4 / CW k-groups of 4 CW column warps. Each warp
+//  * Math: 8 warps, each taking 128 rows x 64 columns of every stage (eight
+//    16-row chunks): 2 / CW k-groups of 4 CW column warps. Each warp
 //    dequantises in registers and runs the legacy-path tensor-core MMA
 //    m16n8k16 with W as the A operand (16 output columns x 16 k) and the
 //    activations as B (16 k x 8 tokens), fp32 accumulators; M is padded to
@@ -742,6 +742,7 @@ uint32_t smem_bytes(const DecodeParams &p) { return (uint32_t)p.stages * p.stage
 struct LaunchInfo {
     int sms = 0;
     cudaError_t err = cudaSuccess;
+    unsigned gen = 0;   // cache generation this was set up in
 };
 
 template <int MT, int CW, bool WG>
@@ -753,9 +754,11 @@ LaunchInfo launch_info()
     LaunchInfo li;
     li.err = cudaGetDevice(&dev);
     if (li.err != cudaSuccess) return li;
+    const unsigned gen = cache_generation();
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(dev);
-    if (it != cache.end()) return it->second;
+    if (it != cache.end() && it->second.gen == gen) return it->second;
+    li.gen = gen;
     auto kern = decode_kernel<MT, CW, WG>;
     li.err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (li.err == cudaSuccess)
@@ -857,6 +860,12 @@ bool decode_supported(int64_t M, int64_t K, int64_t N, int64_t g)
                (int64_t(1) << 30);
 }
 
+int decode_tile_columns(int64_t M, int64_t K, int64_t N, int64_t g)
+{
+    if (!decode_supported(M, K, N, g)) return 0;
+    return wide_tiles(N) ? Geo<2>::kTileCols : Geo<1>::kTileCols;
+}
+
 cudaError_t launch_decode(const Problem &p, cudaStream_t stream)
 {
     if (!decode_supported(p.M, p.K, p.N, p.g)) return cudaErrorInvalidValue;
@@ -892,24 +901,25 @@ static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocWords];
 
 // Device address of g_noalloc_scratch on the current device. Host code only
 // holds a stand-in for the symbol, so the address is looked up once per
-// device (with that device current) and cached.
+// device (with that device current) and cached until awq_shutdown().
 cudaError_t noalloc_scratch_address(uint32_t **out)
 {
     static std::mutex mu;
-    static std::map<int, uint32_t *> addr;
+    static std::map<int, std::pair<uint32_t *, unsigned>> addr;   // device -> (address, generation)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const unsigned gen = cache_generation();
     std::lock_guard<std::mutex> lock(mu);
     auto it = addr.find(dev);
-    if (it != addr.end()) {
-        *out = it->second;
+    if (it != addr.end() && it->second.second == gen) {
+        *out = it->second.first;
         return cudaSuccess;
     }
     uint32_t *ptr = nullptr;
     e = cudaGetSymbolAddress(reinterpret_cast<void **>(&ptr), g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    addr[dev] = ptr;
+    addr[dev] = std::make_pair(ptr, gen);
     *out = ptr;
     return cudaSuccess;
 }

@@ -18,6 +18,7 @@
 // Both check every perm entry: one outside [0, K) writes zeros and records
 // kStatusBadIndex in the device status word instead of reading out of bounds.
 #include <mutex>
+#include <map>
 #include <set>
 
 #include "awq_device.cuh"
@@ -147,14 +148,16 @@ cudaError_t launch_gather_cols(const void *x, int64_t ldx, const int32_t *perm, 
         {
             // the shared-memory limit is a per-device attribute of the function
             static std::mutex mu;
-            static std::set<int> ready;
+            static std::map<int, unsigned> ready;   // device -> cache generation
+            const unsigned gen = cache_generation();
             std::lock_guard<std::mutex> lock(mu);
-            if (!ready.count(dev)) {
+            auto it = ready.find(dev);
+            if (it == ready.end() || it->second != gen) {
                 cudaError_t e = cudaFuncSetAttribute(gather_cols_staged_kernel,
                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                      (int)(kStagedMaxK * 2));
                 if (e != cudaSuccess) return e;
-                ready.insert(dev);
+                ready[dev] = gen;
             }
         }
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

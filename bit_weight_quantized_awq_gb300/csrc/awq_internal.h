@@ -34,6 +34,11 @@ struct Scratch {
     size_t n_counters;
 };
 
+// Bumped by awq_shutdown(): per-device values a launcher caches (symbol
+// addresses, function attributes set once per device) are looked up again
+// when the generation they were cached in is no longer current.
+unsigned cache_generation();
+
 // Returns the address of this device's status word (bit flags, see
 // kStatusTimeout) for kernels to record device-side errors in.
 unsigned int *device_status_word();
@@ -79,6 +84,8 @@ cudaError_t launch_generic(const Problem &p, cudaStream_t stream);
 
 // Decode path (small M). supported_* is host-only shape logic.
 bool decode_supported(int64_t M, int64_t K, int64_t N, int64_t g);
+// columns per decode tile for this shape (0 if the decode kernel cannot serve it)
+int decode_tile_columns(int64_t M, int64_t K, int64_t N, int64_t g);
 cudaError_t launch_decode(const Problem &p, cudaStream_t stream);
 
 // Prefill path (large M, tcgen05).

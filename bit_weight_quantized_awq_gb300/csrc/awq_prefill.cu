@@ -770,6 +770,7 @@ Plan plan_tiles(int64_t M, int64_t K, int64_t N, int sms, int mh)
 struct LaunchInfo {
     int sms = 0;
     cudaError_t err = cudaSuccess;
+    unsigned gen = 0;   // cache generation this was set up in
 };
 
 template <bool kDequant, bool kWhole, int MH>
@@ -781,9 +782,11 @@ LaunchInfo launch_info()
     LaunchInfo li;
     li.err = cudaGetDevice(&dev);
     if (li.err != cudaSuccess) return li;
+    const unsigned gen = cache_generation();
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(dev);
-    if (it != cache.end()) return it->second;
+    if (it != cache.end() && it->second.gen == gen) return it->second;
+    li.gen = gen;
     li.err = cudaFuncSetAttribute(prefill_kernel<kDequant, kWhole, MH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   Cfg<kDequant, MH>::kSmemBytes);
     if (li.err == cudaSuccess)

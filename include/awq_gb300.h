@@ -150,6 +150,16 @@ int awq_select_path(int64_t M, int64_t K, int64_t N, int64_t group_size);
 int awq_forward_launches(int64_t M, int64_t K, int64_t N, int64_t group_size, awq_path_t path);
 
 /*
+ * awq_decode_tile_columns -- the output-column width of one tile of the decode
+ * kernel (AWQ_PATH_DECODE) for this shape: 512 when N is a multiple of 512 and
+ * at least 32768 (rows of 256 bytes of packed weights), else 256. Returns 0 if
+ * the decode kernel cannot serve the shape and -1 for an invalid shape.
+ * Host-only, no CUDA call. Tests use it to check that a shape reaches the
+ * kernel variant they mean to exercise.
+ */
+int awq_decode_tile_columns(int64_t M, int64_t K, int64_t N, int64_t group_size);
+
+/*
  * awq_dequant -- unpack and dequantise the packed weights (the per-group
  * dequantisation of the WQLinear page, Description, __init__ bullet 3):
  *   W[k, n] = fp16_rn((q[k, n] - z[k / g, n]) * scales[k / g, n])
@@ -341,15 +351,23 @@ const char *awq_status_string(awq_status_t status);
 /*
  * awq_last_device_status -- synchronises `stream`, then reads and clears the
  * current device's status word. Returns AWQ_OK, AWQ_ERR_TIMEOUT if a kernel's
- * bounded wait ran out since the last read (that kernel wrote no result and
- * the scratch area of the stream it ran on is reset), AWQ_ERR_INVALID_ARG if
- * a g_idx entry was outside [0, G), or AWQ_ERR_CUDA if the synchronisation
- * itself failed.
+ * bounded wait ran out since the last read, AWQ_ERR_INVALID_ARG if a g_idx
+ * entry was outside [0, G), or AWQ_ERR_CUDA if a synchronisation or reset
+ * failed.
+ *
+ * After a timeout: the kernel that gave up wrote no result, and it may have
+ * left split-K arrival counters of its stream non-zero. Results of later
+ * decode-path calls on that device are not to be trusted until this call
+ * has returned AWQ_ERR_TIMEOUT: it then synchronises the whole device and
+ * zeroes, in place, the counters of every stream's scratch area (the areas
+ * stay allocated, so CUDA graphs captured earlier remain valid).
  */
 awq_status_t awq_last_device_status(awq_stream_t stream);
 
-/* Frees every scratch area the library allocated, on every device. Call it
- * only when no call of this library is in flight. Later calls allocate again. */
+/* Frees every scratch area the library allocated, on every device, and drops
+ * the per-device values the library caches (symbol addresses, kernel
+ * attributes). Call it only when no call of this library is in flight, and
+ * after a cudaDeviceReset before the next call. Later calls set up again. */
 void awq_shutdown(void);
 
 #ifdef __cplusplus

@@ -222,3 +222,18 @@ def test_missing_library_fails_loudly(tmp_path):
             f"b.load_library({str(tmp_path / 'nope.so')!r})\n")
     r = subprocess.run(["python", "-c", code], cwd=ROOT, capture_output=True, text=True)
     assert r.returncode != 0 and "not found" in r.stderr
+
+
+def test_decode_tile_columns_plan(lib):
+    """Host-only plan query: 512-column decode tiles exactly when N is a
+    multiple of 512 and at least 32768; 0 where the decode kernel does not
+    serve the shape; -1 for an invalid shape."""
+    q = awq.awq_decode_tile_columns
+    assert q(1, 4096, 32768, 128) == 512
+    assert q(32, 2112, 33280, 96) == 512
+    assert q(1, 4096, 32256, 128) == 256      # a multiple of 512, below 32768
+    assert q(1, 4096, 33024, 128) == 256      # at least 32768, not a multiple of 512
+    assert q(16, 4096, 22016, 128) == 256
+    assert q(33, 4096, 4096, 128) == 0        # more rows than the decode kernel takes
+    assert q(1, 4096, 8, -1) == 0             # N below one 32-column TMA row
+    assert q(1, 4096, 12, 128) == -1          # N % 8 != 0

@@ -111,9 +111,33 @@ def test_ragged_and_edge_shapes(gpu, M, K, N, g, bias):
     check_problem(make_problem(M, K, N, g, bias=bias, seed=M))
 
 
-# Decode on 512-column tiles (N a multiple of 512 and at least 8192): a
-# ragged last k-stage (K % 128 == 64), groups that split a warp's 64 rows
-# (g = 32, 96), both token tiles (M <= 8 and 9..16), with and without bias.
+# Decode on 512-column tiles (N a multiple of 512 and at least 32768): a
+# ragged last k-stage (K % 128 == 64, the 512-column stage holds 128 rows),
+# groups that split a warp's rows (g = 32, 64, 96), each token-tile class
+# (M <= 8, 9..16, 17..32), with and without bias. The host plan query checks
+# that each shape really takes 512-column tiles; the oracle is compared on
+# every row and on column blocks at the start, the middle and the ragged end.
+WIDE_TILE_CASES = [
+    (1, 1088, 32768, 32, True),
+    (8, 4160, 33280, 64, False),
+    (9, 2112, 32768, 96, True),
+    (16, 1088, 40960, 32, False),
+    (17, 4160, 32768, 64, True),
+    (32, 2112, 33280, 96, False),
+    (3, 4096, 32768, 128, True),     # whole groups, K a multiple of the stage
+]
+
+
+@pytest.mark.parametrize("M,K,N,g,bias", WIDE_TILE_CASES)
+def test_wide_tile_decode(gpu, M, K, N, g, bias):
+    from bit_weight_quantized_awq_gb300 import awq_decode_tile_columns
+    assert awq_decode_tile_columns(M, K, N, g) == 512
+    check_problem(make_problem(M, K, N, g, bias=bias, seed=M + 100), paths=[Path.DECODE, Path.AUTO],
+                  full=False)
+
+
+# The same split-group and ragged-stage cases on 256-column tiles (N below
+# 32768), every output compared.
 @pytest.mark.parametrize("M,K,N,g,bias", [
     (1, 1088, 8192, 32, True),
     (9, 2112, 8704, 96, False),
@@ -121,7 +145,9 @@ def test_ragged_and_edge_shapes(gpu, M, K, N, g, bias):
     (3, 4096, 8192, 128, True),
     (12, 11008, 12288, 128, True),
 ])
-def test_wide_tile_decode(gpu, M, K, N, g, bias):
+def test_narrow_tile_decode(gpu, M, K, N, g, bias):
+    from bit_weight_quantized_awq_gb300 import awq_decode_tile_columns
+    assert awq_decode_tile_columns(M, K, N, g) == 256
     check_problem(make_problem(M, K, N, g, bias=bias, seed=M + 100), full=K * N <= 4160 * 16384)
 
 

@@ -81,8 +81,8 @@ def test_reference_arm_line_on_one_rank(monkeypatch, capsys):
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["metric"] == bench.METRIC
     assert d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3
-    assert d["value"] > 0 and d["higher_is_better"] is True and d["unit"] == "weight GB/s"
-    assert d["config"]["workload"] == "decode-7b" and d["data"] == "synthetic"
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["unit"] == "TFLOP/s"
+    assert d["config"]["workload"] == bench.DEFAULT_WORKLOAD and d["data"] == "synthetic"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}

@@ -4,9 +4,10 @@ It exists for callers that must not have device memory allocated behind
 their back -- serving processes that budget all device memory up front, or
 frameworks whose caching allocator owns the GPU -- and keeps the decode
 kernel's split-K scratch in one array compiled into the library. These tests
-call it through the C ABI and compare it with the regular entry point,
-awq_linear_forward, within the suite's tolerance (1e-3 + 4e-3 |y|), on calls
-made back to back: the second call finds the array as the first one left it.
+call it through the C ABI on calls made back to back (the second call finds
+the array as the first one left it) and compare every output with the CPU
+oracle on the same seeded inputs, and with the regular entry point,
+awq_linear_forward, both within the suite's tolerance (1e-3 + 4e-3 |y|).
 
 This file is named so that pytest collects it last; it passes on its own in
 a fresh process as well as after the rest of the suite.
@@ -16,6 +17,7 @@ import pytest
 import torch
 
 import bit_weight_quantized_awq_gb300 as awq
+import oracle
 from bit_weight_quantized_awq_gb300 import Status
 from bit_weight_quantized_awq_gb300.build import build
 from bit_weight_quantized_awq_gb300.synthetic import make_problem
@@ -37,17 +39,21 @@ def test_noalloc_matches_regular_entry_point_on_consecutive_calls(gpu):
              make_problem(16, 4096, 12288, 128, bias=False, seed=32),
              make_problem(1, 1024, 800, 64, bias=True, seed=33)]
     probs = [c.to("cuda") for c in cases]
+    refs = [oracle.forward(c.x.numpy(), c.qweight.numpy(), c.qzeros.numpy(), c.scales.numpy(),
+                           None if c.bias is None else c.bias.numpy(), c.group_size) for c in cases]
     # back to back: A, A again, then B and C, each checked against the
-    # regular entry point on the same inputs
-    for p in [probs[0], probs[0], probs[1], probs[2]]:
-        y_ref = torch.empty((p.M, p.N), dtype=torch.float16, device="cuda")
+    # oracle and against the regular entry point on the same inputs
+    for i in [0, 0, 1, 2]:
+        p = probs[i]
+        y_reg = torch.empty((p.M, p.N), dtype=torch.float16, device="cuda")
         y_new = torch.full((p.M, p.N), float("nan"), dtype=torch.float16, device="cuda")
-        assert _call(awq.awq_linear_forward, p, y_ref, stream) == Status.OK
         assert _call(awq.awq_linear_forward_decode_noalloc, p, y_new, stream) == Status.OK
+        assert _call(awq.awq_linear_forward, p, y_reg, stream) == Status.OK
         torch.cuda.synchronize()
-        ref = y_ref.double().cpu().numpy()
         new = y_new.double().cpu().numpy()
-        assert np.all(np.abs(new - ref) <= ATOL + RTOL * np.abs(ref)), (p.M, p.K, p.N)
+        reg = y_reg.double().cpu().numpy()
+        assert np.all(np.abs(new - refs[i]) <= ATOL + RTOL * np.abs(refs[i])), ("oracle", p.M, p.K, p.N)
+        assert np.all(np.abs(new - reg) <= ATOL + RTOL * np.abs(reg)), ("regular", p.M, p.K, p.N)
     assert awq.awq_last_device_status(stream) == Status.OK
 
 
