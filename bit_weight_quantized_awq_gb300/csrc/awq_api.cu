@@ -16,6 +16,9 @@
 #include <cuda_runtime.h>
 
 #include "../../include/awq_gb300.h"
+#ifdef AWQ_FAULT_TEST
+#include "../../include/awq_gb300_fault_test.h"
+#endif
 #include "awq_internal.h"
 
 namespace awq {
@@ -164,6 +167,11 @@ static cudaError_t reset_scratch_counters(int dev)
 }
 
 std::atomic<unsigned> g_cache_generation{1};
+
+#ifdef AWQ_FAULT_TEST
+std::atomic<int> g_fault_injection{0};
+int fault_injection() { return g_fault_injection.load(std::memory_order_acquire); }
+#endif
 
 unsigned cache_generation() { return g_cache_generation.load(std::memory_order_acquire); }
 
@@ -542,6 +550,13 @@ awq_status_t awq_last_device_status(awq_stream_t stream)
     if (word & awq::kStatusBadIndex) return AWQ_ERR_INVALID_ARG;
     return AWQ_ERR_CUDA;
 }
+
+#ifdef AWQ_FAULT_TEST
+void awq_test_inject_fault(int on)
+{
+    awq::g_fault_injection.store(on ? 1 : 0, std::memory_order_release);
+}
+#endif
 
 void awq_shutdown(void)
 {

@@ -71,32 +71,46 @@ constexpr int kMaxTokens = 32;
 constexpr int kMaxGroupRows = 8;     // group rows one stage may touch
 constexpr int kWBytes = 32768;       // packed weights per stage
 constexpr int kMaxStages = 8;
-constexpr int kConsumerWarps = 8;    // dequantise + MMA
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;   // + one TMA producer warp
+// Warps that dequantise and multiply (plus one TMA producer warp), by the
+// number MT of 8-token tiles: more warps per SM sub-partition hide more of
+// the load and instruction latencies; a thread of a CTA of W warps gets at
+// most 65536 / (32 W) registers.
+constexpr int kConsumerWarpsOneTile = 8;
+template <int MT>
+struct Warps {
+    static constexpr int kConsumer = MT == 1 ? kConsumerWarpsOneTile : 8;
+    static constexpr int kConsumerThreads = kConsumer * 32;
+    static constexpr int kThreads = kConsumerThreads + 32;
+};
 constexpr int kBarBytes = 2 * kMaxStages * 8 + 64;   // full/empty barriers + flags
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kMaxTileCols = 512;
 constexpr int kMaxPartialFloats = kMaxTokens * kMaxTileCols;  // one partial slot
 
-// Tile geometry for CW 128-byte chunks of packed words per weight row.
-template <int CW>
+// Tile geometry for CW 128-byte chunks of packed words per weight row and
+// NW consumer warps.
+template <int CW, int NW = 8>
 struct Geo {
     static constexpr int kTileWords = 32 * CW;
     static constexpr int kTileCols = 256 * CW;
     static constexpr int kStageRows = kWBytes / (kTileWords * 4);
     static constexpr int kKBlocks = kStageRows / 64;     // 64-row blocks of a stage
     static constexpr int kColWarps = 4 * CW;                      // warps across a tile (64 columns each)
-    static constexpr int kKGroups = kConsumerWarps / kColWarps;   // warps down a stage
+    static constexpr int kKGroups = NW / kColWarps;               // warps down a stage
     static constexpr int kRowsPerWarp = kStageRows / kKGroups;    // 128
     static constexpr int kChunksPerWarp = kRowsPerWarp / 16;
     static_assert(kKGroups * kRowsPerWarp == kStageRows, "warps must cover a stage");
 };
-static_assert(Geo<1>::kKGroups == 2, "CW = 1 folds one k-group");
-static_assert(Geo<2>::kKGroups == 1, "CW = 2 has nothing to fold");
-// A k-group's fp32 sums, 16 MT x 128 floats, fit a CW = 1 slot's weight
-// area (32 KB) for every MT <= 4.
-static_assert(16 * (kMaxTokens / 8) * Geo<1>::kColWarps * 32 * 4 <= kWBytes, "fold buffer fits a slot");
+// The fp32 sums of every k-group but the first, 16 MT floats per thread,
+// fit the weight area (32 KB) of the slot they are folded through.
+template <int MT, int CW>
+constexpr bool fold_fits()
+{
+    using G = Geo<CW, Warps<MT>::kConsumer>;
+    return (G::kKGroups - 1) * 16 * MT * G::kColWarps * 32 * 4 <= kWBytes;
+}
+static_assert(fold_fits<1, 1>() && fold_fits<2, 1>() && fold_fits<4, 1>() && fold_fits<1, 2>() &&
+                  fold_fits<2, 2>() && fold_fits<4, 2>(), "fold buffer fits a slot");
 
 struct DecodeParams {
     const __half *bias;
@@ -111,6 +125,9 @@ struct DecodeParams {
     uint32_t stage_bytes;   // bytes per slot (multiple of 1024)
     uint32_t x_off, s_off, z_off;  // activation / scale / zero rows inside a slot
     uint32_t stage_tx;      // bytes one stage's TMA boxes deliver
+#ifdef AWQ_FAULT_TEST
+    int fault;              // CTA 0's producer issues nothing (fault-test build only)
+#endif
 };
 
 __device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
@@ -153,12 +170,14 @@ __device__ __forceinline__ void fold_add(const float *src, float (&acc)[4][MT][4
 }
 
 template <int MT, int CW, bool kWholeGroups>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Warps<MT>::kThreads, 1)
 decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
               const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
               const DecodeParams p)
 {
-    using G = Geo<CW>;
+    constexpr int kConsumerWarps = Warps<MT>::kConsumer;
+    constexpr int kConsumerThreads = Warps<MT>::kConsumerThreads;
+    using G = Geo<CW, kConsumerWarps>;
     constexpr int kTileCols = G::kTileCols;
     constexpr int kTileWords = G::kTileWords;
     constexpr int kStageRows = G::kStageRows;
@@ -249,7 +268,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             // The weights, scales and zero points of the first S stages do
             // not depend on the kernel before this one: load them while it
             // finishes, and the activations once it has.
-            const int pre = n_iters < S ? n_iters : S;
+            int pre = n_iters < S ? n_iters : S;
+#ifdef AWQ_FAULT_TEST
+            // injected fault: nothing is loaded, so the consumers' bounded
+            // waits on the first stage run out
+            if (p.fault && c == 0) {
+                ptx::wait_prerequisites();
+                return;
+            }
+#endif
             const int kb_first = kb;
             for (int i = 0; i < pre; ++i) {
                 issue_weights();
@@ -452,15 +479,20 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         }
 
         if (seg_end) {
-            if (KG == 2) {
-                // ---- fold k-group 1 into k-group 0 through this slot's weight
-                //      area (every warp has finished reading it at the first
-                //      barrier), then release the slot
+            if (KG >= 2) {
+                // ---- fold k-groups 1 .. KG - 1 into k-group 0, in that order,
+                //      through this slot's weight area (every warp has
+                //      finished reading it at the first barrier), then
+                //      release the slot
                 float *red = reinterpret_cast<float *>(stp);
+                constexpr int kRegion = 16 * MT * kKGroupThreads;
                 ptx::named_barrier(1, kConsumerThreads);
-                if (kg == 1) fold_store<MT, kKGroupThreads>(red, acc, ct);
+                if (kg >= 1) fold_store<MT, kKGroupThreads>(red + (kg - 1) * kRegion, acc, ct);
                 ptx::named_barrier(1, kConsumerThreads);
-                if (kg == 0) fold_add<MT, kKGroupThreads>(red, acc, ct);
+                if (kg == 0) {
+#pragma unroll
+                    for (int q = 1; q < KG; ++q) fold_add<MT, kKGroupThreads>(red + (q - 1) * kRegion, acc, ct);
+                }
                 // generic-proxy accesses to the slot are ordered before the
                 // TMA writes that refill it
                 ptx::fence_proxy_async_smem();
@@ -760,6 +792,7 @@ LaunchInfo launch_info()
     if (it != cache.end() && it->second.gen == gen) return it->second;
     li.gen = gen;
     auto kern = decode_kernel<MT, CW, WG>;
+    constexpr int kThreads = Warps<MT>::kThreads;
     li.err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (li.err == cudaSuccess)
         li.err = cudaDeviceGetAttribute(&li.sms, cudaDevAttrMultiProcessorCount, dev);
@@ -792,6 +825,9 @@ cudaError_t prepare(const Problem &pr, int max_ctas, CUtensorMap *maps, DecodePa
     p->status = device_status_word();
     p->M = (int)pr.M; p->K = (int)pr.K; p->N = (int)pr.N; p->g = (int)pr.g;
     p->tiles = tiles; p->kiters = kiters; p->total = (int)total; p->ctas = ctas;
+#ifdef AWQ_FAULT_TEST
+    p->fault = fault_injection();
+#endif
     return cudaSuccess;
 }
 
@@ -800,7 +836,7 @@ cudaError_t launch_kernel(const CUtensorMap *maps, const DecodeParams &p, cudaSt
 {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)p.ctas);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Warps<MT>::kThreads);
     cfg.dynamicSmemBytes = smem_bytes(p);
     cfg.stream = stream;
     // programmatic dependent launch: the kernel starts streaming weights while

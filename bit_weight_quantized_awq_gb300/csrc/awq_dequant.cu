@@ -6,9 +6,14 @@
 //
 // HBM-bound elementwise work: per packed int32 read (4 B) it writes 8 fp16
 // (16 B); scales and zero points are re-read by the g rows of a group and stay
-// in L2. One thread handles one packed word: a coalesced 4-byte load and one
-// 16-byte store per thread. The grid is a multiple of the SM count and
-// strides over the K x N/8 words.
+// in L2. dequant_vec_kernel (rows of a multiple of four packed words): each
+// thread takes four consecutive packed words of one row with one 16-byte
+// load, their zero-point words with one 16-byte load and their 32 scales
+// with four, converts them two weights per half2 instruction
+// (dequant_word_h2), and stores 64 contiguous bytes; two such groups are in
+// flight per thread before either is used. dequant_kernel takes one word per
+// thread for any other width (N % 32 != 0). The grids are a multiple of the
+// SM count and stride over the words.
 #include "awq_device.cuh"
 #include "awq_internal.h"
 
@@ -48,6 +53,59 @@ dequant_kernel(const uint32_t *__restrict__ qweight, const uint32_t *__restrict_
         *reinterpret_cast<uint4 *>(s) = sraw;
         dequant_word(qw, zw, s, w);
         *reinterpret_cast<uint4 *>(W + dst * 8) = *reinterpret_cast<const uint4 *>(w);
+    }
+}
+
+// Four consecutive packed words per thread (window width and start multiples
+// of four words): quads q = idx of the [K, wwords / 4] array of word quads.
+__global__ void __launch_bounds__(256)
+dequant_vec_kernel(const uint32_t *__restrict__ qweight, const uint32_t *__restrict__ qzeros,
+                   const __half *__restrict__ scales, __half *__restrict__ W,
+                   int64_t K, int64_t words, int64_t g, int64_t word0, int64_t wwords,
+                   const int32_t *__restrict__ row_out, unsigned int *status)
+{
+    const int64_t wq = wwords / 4;        // quads per output row
+    const int64_t total = K * wq;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t base = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; base < total; base += 2 * stride) {
+        uint4 qv[2], zv[2], sv[2][4];
+        int64_t dst[2];
+        bool live[2];
+        // issue every load of both quads before any arithmetic
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t idx = base + u * stride;
+            live[u] = idx < total;
+            if (!live[u]) continue;
+            const int64_t k = idx / wq;
+            const int64_t jq = idx - k * wq;
+            const int64_t j = word0 + 4 * jq;     // first packed word of the quad
+            dst[u] = idx;
+            if (row_out) {
+                const int64_t r = __ldg(row_out + k);
+                if (r < 0 || r >= K) {
+                    raise_status(status, kStatusBadIndex);
+                    live[u] = false;
+                    continue;
+                }
+                dst[u] = r * wq + jq;
+            }
+            const int64_t gi = k / g;
+            qv[u] = __ldg(reinterpret_cast<const uint4 *>(qweight + k * words + j));
+            zv[u] = __ldg(reinterpret_cast<const uint4 *>(qzeros + gi * words + j));
+            const uint4 *sp = reinterpret_cast<const uint4 *>(scales + (gi * words + j) * 8);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) sv[u][w] = __ldg(sp + w);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (!live[u]) continue;
+            uint4 *out = reinterpret_cast<uint4 *>(W + dst[u] * 32);
+            out[0] = dequant_word_h2(qv[u].x, zv[u].x, sv[u][0]);
+            out[1] = dequant_word_h2(qv[u].y, zv[u].y, sv[u][1]);
+            out[2] = dequant_word_h2(qv[u].z, zv[u].z, sv[u][2]);
+            out[3] = dequant_word_h2(qv[u].w, zv[u].w, sv[u][3]);
+        }
     }
 }
 
@@ -106,10 +164,22 @@ cudaError_t launch_dequant_cols(const Problem &p, int64_t c0, int64_t nc, void *
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t words = p.N / 8;
-    const int64_t total = p.K * (nc / 8);
     const int threads = 256;
-    int64_t blocks = (total + threads - 1) / threads;
     const int64_t cap = (int64_t)(sms > 0 ? sms : 1) * 8;
+    if (words % 4 == 0 && (c0 / 8) % 4 == 0 && (nc / 8) % 4 == 0) {
+        // 16-byte rows of packed words: four words per thread, two quads in flight
+        const int64_t quads = p.K * (nc / 32);
+        int64_t blocks = (quads + 2 * threads - 1) / (2 * threads);
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) return cudaSuccess;
+        dequant_vec_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
+            reinterpret_cast<const uint32_t *>(p.qweight), reinterpret_cast<const uint32_t *>(p.qzeros),
+            static_cast<const __half *>(p.scales), static_cast<__half *>(W), p.K, words, p.g, c0 / 8,
+            nc / 8, p.row_perm, device_status_word());
+        return cudaGetLastError();
+    }
+    const int64_t total = p.K * (nc / 8);
+    int64_t blocks = (total + threads - 1) / threads;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) return cudaSuccess;
     dequant_kernel<<<(unsigned)blocks, threads, 0, stream>>>(

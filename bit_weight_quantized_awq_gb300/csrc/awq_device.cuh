@@ -39,6 +39,42 @@ __device__ __forceinline__ void dequant_word(uint32_t qword, uint32_t zword,
         w[i] = dequant_one(nibble(qword, i), nibble(zword, i), s[i]);
 }
 
+// The same eight weights with half2 arithmetic: two weights per instruction.
+// One LOP3 puts the nibbles of columns c and c + 4 (c = 0..3; bytes 0 and 2
+// of the word, or of the word shifted right by 8) into the low fraction bits
+// of 1024.0 (low nibble of a byte) or bits 4..7 of 64.0 (high nibble: the
+// fraction step of 64.0 is 1/16, so the value is 64 + code), the same for the
+// zero word, then one exact half2 subtraction and one half2 multiply that
+// rounds once -- exactly dequant_one on each lane. Result in column order:
+// out[p] holds columns 2p and 2p + 1 (low half first), i.e. the 16 bytes of
+// the eight fp16 weights as they lie in memory.
+__device__ __forceinline__ uint4 dequant_word_h2(uint32_t v, uint32_t zw, uint4 sraw) {
+    const uint32_t vh = v >> 8, zh = zw >> 8;
+    // scale pairs (s0, s4) (s1, s5) (s2, s6) (s3, s7)
+    const uint32_t s04 = __byte_perm(sraw.x, sraw.z, 0x5410), s15 = __byte_perm(sraw.x, sraw.z, 0x7632);
+    const uint32_t s26 = __byte_perm(sraw.y, sraw.w, 0x5410), s37 = __byte_perm(sraw.y, sraw.w, 0x7632);
+    const uint32_t lo = 0x64006400u, hi = 0x54005400u;
+    __half2 q, z, r04, r15, r26, r37;
+    uint32_t t;
+    t = (v & 0x000F000Fu) | lo; q = *reinterpret_cast<__half2 *>(&t);
+    t = (zw & 0x000F000Fu) | lo; z = *reinterpret_cast<__half2 *>(&t);
+    r04 = __hmul2_rn(__hsub2(q, z), *reinterpret_cast<const __half2 *>(&s04));
+    t = (v & 0x00F000F0u) | hi; q = *reinterpret_cast<__half2 *>(&t);
+    t = (zw & 0x00F000F0u) | hi; z = *reinterpret_cast<__half2 *>(&t);
+    r15 = __hmul2_rn(__hsub2(q, z), *reinterpret_cast<const __half2 *>(&s15));
+    t = (vh & 0x000F000Fu) | lo; q = *reinterpret_cast<__half2 *>(&t);
+    t = (zh & 0x000F000Fu) | lo; z = *reinterpret_cast<__half2 *>(&t);
+    r26 = __hmul2_rn(__hsub2(q, z), *reinterpret_cast<const __half2 *>(&s26));
+    t = (vh & 0x00F000F0u) | hi; q = *reinterpret_cast<__half2 *>(&t);
+    t = (zh & 0x00F000F0u) | hi; z = *reinterpret_cast<__half2 *>(&t);
+    r37 = __hmul2_rn(__hsub2(q, z), *reinterpret_cast<const __half2 *>(&s37));
+    const uint32_t a = *reinterpret_cast<uint32_t *>(&r04), b = *reinterpret_cast<uint32_t *>(&r15);
+    const uint32_t c = *reinterpret_cast<uint32_t *>(&r26), d = *reinterpret_cast<uint32_t *>(&r37);
+    // back to column order: (0,1) (2,3) (4,5) (6,7)
+    return make_uint4(__byte_perm(a, b, 0x5410), __byte_perm(c, d, 0x5410), __byte_perm(a, b, 0x7632),
+                      __byte_perm(c, d, 0x7632));
+}
+
 // Record a device-side error in the status word.
 __device__ __forceinline__ void raise_status(unsigned int *status, unsigned int bits) {
     if (status) atomicOr(status, bits);
@@ -105,7 +141,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // clock cycles (about 2 s at 2 GHz, longer at lower clocks) records
 // AWQ_ERR_TIMEOUT in the status word and gives up. The limit is kept with the
 // SM-local cycle counter: reading %globaltimer costs far more than a poll.
+#ifdef AWQ_FAULT_TEST
+// the fault-test build of the library (tests only): about 2 ms, so that a
+// test that makes a wait run out finishes quickly
+constexpr long long kWaitLimitCycles = 4000000ll;
+#else
 constexpr long long kWaitLimitCycles = 4000000000ll;
+#endif
 
 // Bounded wait on an mbarrier phase. Returns false if the wait gave up,
 // either because its own limit ran out or because another thread of the CTA

@@ -39,6 +39,13 @@ struct Scratch {
 // when the generation they were cached in is no longer current.
 unsigned cache_generation();
 
+#ifdef AWQ_FAULT_TEST
+// Fault-test build only: when non-zero, the next decode and prefill launches
+// tell CTA 0's TMA producer to issue nothing, so that the waits of that CTA's
+// consumers on the stage barriers run out (see awq_gb300_fault_test.h).
+int fault_injection();
+#endif
+
 // Returns the address of this device's status word (bit flags, see
 // kStatusTimeout) for kernels to record device-side errors in.
 unsigned int *device_status_word();

@@ -141,6 +141,9 @@ struct PrefillParams {
     int sk_tiles;           // tiles after those, split along k between sk_ctas CTAs
     int sk_ctas;
     uint32_t stage_tx;
+#ifdef AWQ_FAULT_TEST
+    int fault;              // CTA 0's producer issues nothing (fault-test build only)
+#endif
 };
 
 // One stream-K partial: 128 rows x 256 accumulator columns, fp32, laid out
@@ -315,6 +318,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             }
             int it = 0, issued = 0;
             bool ok = true;
+#ifdef AWQ_FAULT_TEST
+            // injected fault: nothing is loaded, so the bounded waits of the
+            // MMA, dequant and epilogue warps on the first stage run out
+            if (p.fault && blockIdx.x == 0) ok = false;
+#endif
             for (int si = 0; si < sg.count && ok; ++si) {
                 int tile, kb0, kb1;
                 sg.get(p, si, tile, kb0, kb1);
@@ -835,6 +843,9 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int6
     p.y = static_cast<__half *>(pr.y);
     p.y32 = pr.y32;
     p.status = device_status_word();
+#ifdef AWQ_FAULT_TEST
+    p.fault = fault_injection();
+#endif
     p.M = M; p.K = K; p.N = N; p.g = g;
     p.ldy = ldy > 0 ? ldy : N;
     p.tiles_m = tiles_m; p.tiles_n = tiles_n; p.kiters = kiters;

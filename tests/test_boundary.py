@@ -237,3 +237,17 @@ def test_decode_tile_columns_plan(lib):
     assert q(33, 4096, 4096, 128) == 0        # more rows than the decode kernel takes
     assert q(1, 4096, 8, -1) == 0             # N below one 32-column TMA row
     assert q(1, 4096, 12, 128) == -1          # N % 8 != 0
+
+
+def test_fault_test_build_exports_the_switch_and_the_main_library_does_not(lib):
+    """The timeout switch exists only in the fault-test build, which the GPU
+    timeout tests load; the library users link has no such symbol."""
+    from bit_weight_quantized_awq_gb300.build import FAULT_LIB
+    main = subprocess.run(["nm", "-D", "--defined-only", awq.LIB_PATH], capture_output=True,
+                          text=True, check=True).stdout
+    ft = subprocess.run(["nm", "-D", "--defined-only", FAULT_LIB], capture_output=True,
+                        text=True, check=True).stdout
+    assert "awq_test_inject_fault" not in main
+    assert re.search(r"\sT\sawq_test_inject_fault\b", ft)
+    for n in awq.EXPORTED:
+        assert re.search(rf"\sT\s{n}\b", ft), n
