@@ -741,17 +741,23 @@ struct Plan {
 
 // Row blocks per band of the tile order. Whole waves in row-fastest order
 // sweep all of x once per wave. When x is larger than a share of L2, bands
-// of as many row blocks as fit that share are used instead, provided a band
-// still spans at least a wave of tiles: x is then read about once and the
-// weights once per band.
+// of as many row blocks as fit that share are used instead -- and at least
+// as many as make a band span a wave of tiles, so that a wave takes all the
+// column blocks of a few row blocks: the CTAs of a wave walk k in step, so
+// a wave reads each of its blocks of x and of W from DRAM about once, and
+// over the whole launch x is read about once and the weights once per
+// band. (Row-fastest waves of a tall x instead read all of x in every wave:
+// 846 MB for 338 MB of operands at M = 8192, K = 11008, N = 4096.)
 constexpr int64_t kL2Share = 32ll << 20;
 
 int group_rows(int tiles_m, int tiles_n, int64_t K, int sms, int mh)
 {
     const int64_t x_block = (int64_t)BM * mh * K * 2;      // one row block of x
     if ((int64_t)tiles_m * x_block <= kL2Share) return tiles_m;
-    const int64_t gm = kL2Share / x_block;
-    if (gm < 1 || gm * tiles_n < sms) return tiles_m;
+    int64_t gm = kL2Share / x_block;
+    const int64_t wave_rows = (sms + tiles_n - 1) / tiles_n;   // row blocks that span a wave
+    if (gm < wave_rows) gm = wave_rows;
+    if (gm >= tiles_m) return tiles_m;
     return (int)gm;
 }
 

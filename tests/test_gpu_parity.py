@@ -169,12 +169,17 @@ def test_prefill_stream_k(gpu, M, K, N, g, bias):
         assert torch.equal(run_path(pg, Path.PREFILL).view(torch.int16), y0.view(torch.int16))
 
 
-# x larger than the L2 share the tile order plans for: 18 row blocks of 256
-# in bands of 16 (the last band 2 rows high) times 10 column blocks, on the
-# fused kernel and on the GEMM core; sampled rows and column blocks.
+# x larger than the L2 share the tile order plans for, on the fused kernel
+# and on the GEMM core; sampled rows and column blocks:
+#  * K = 4096, N = 2560: 18 row blocks of 256 in bands of 16 (the share
+#    holds 16 row blocks; the last band is 2 rows high) x 10 column blocks;
+#  * K = 11008, N = 4096: the share holds only 5 row blocks, fewer than a
+#    wave needs with 16 column blocks, so bands are 10 row blocks high (the
+#    last one 8).
 @pytest.mark.parametrize("path", [Path.PREFILL, Path.DEQUANT_GEMM])
-def test_banded_tile_order(gpu, path):
-    check_problem(make_problem(4608, 4096, 2560, 128, bias=True, seed=4608), paths=[path], full=False)
+@pytest.mark.parametrize("K,N", [(4096, 2560), (11008, 4096)])
+def test_banded_tile_order(gpu, path, K, N):
+    check_problem(make_problem(4608, K, N, 128, bias=True, seed=4608), paths=[path], full=False)
 
 
 # --------------------------------------------------------------------------
