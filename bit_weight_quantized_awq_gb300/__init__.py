@@ -30,6 +30,7 @@ from ._binding import (  # noqa: F401
     awq_path_supported,
     awq_permute_rows,
     awq_quantize_rtn,
+    awq_reserve,
     awq_select_path,
     awq_forward_launches,
     awq_shutdown,

@@ -38,7 +38,11 @@ EXPORTED = (
     "awq_gidx_sort",
     "awq_permute_rows",
     "awq_linear_forward_sorted",
+    "awq_reserve",
 )
+
+RESERVE_SORTED = 1
+RESERVE_GIDX = 2
 
 
 class Status(enum.IntEnum):
@@ -125,6 +129,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.awq_pack.restype = _INT
         lib.awq_quantize_rtn.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P]
         lib.awq_quantize_rtn.restype = _INT
+        lib.awq_reserve.argtypes = [_I64, _I64, _I64, ctypes.c_uint, _P]
+        lib.awq_reserve.restype = _INT
         lib.awq_shutdown.argtypes = []
         lib.awq_shutdown.restype = None
         _lib = lib
@@ -214,6 +220,10 @@ def awq_status_string(status) -> str:
 
 def awq_last_device_status(stream) -> int:
     return load_library().awq_last_device_status(stream)
+
+
+def awq_reserve(max_M, max_K, max_N, flags, stream) -> int:
+    return load_library().awq_reserve(max_M, max_K, max_N, flags, stream)
 
 
 def awq_shutdown() -> None:

@@ -6,6 +6,7 @@
 // the ABI has no other width), out_features = 8 x qweight columns so
 // N % 8 == 0, group_size -1 means K, and K % group_size == 0. Where the page
 // asserts, this layer returns a status instead; nothing aborts.
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <map>
@@ -44,7 +45,11 @@ struct ScratchEntry {
     size_t w16_bytes = 0;
     void *xs = nullptr;            // activations in sorted row order (act-order forward)
     size_t xs_bytes = 0;
+    bool reserved = false;         // sized by awq_reserve: never grows afterwards
 };
+
+// set when a call needed more scratch than its stream's reservation
+thread_local bool t_over_reservation = false;
 std::map<std::pair<int, cudaStream_t>, ScratchEntry> g_scratch;
 
 } // namespace
@@ -69,6 +74,10 @@ bool get_scratch(cudaStream_t stream, size_t partial_floats, size_t n_counters, 
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     std::lock_guard<std::mutex> lock(g_mutex);
     ScratchEntry &e = g_scratch[std::make_pair(dev, stream)];
+    if (e.reserved && (e.partial_floats < partial_floats || e.n_counters < n_counters)) {
+        t_over_reservation = true;
+        return false;
+    }
     if (e.partial_floats < partial_floats) {
         // the old area may still be read by work queued on this stream
         if (e.partials) {
@@ -118,6 +127,10 @@ bool grow_area(cudaStream_t stream, size_t bytes, void *ScratchEntry::*ptr, size
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     std::lock_guard<std::mutex> lock(g_mutex);
     ScratchEntry &e = g_scratch[std::make_pair(dev, stream)];
+    if (e.reserved && e.*cap < bytes) {
+        t_over_reservation = true;
+        return false;
+    }
     if (e.*cap < bytes) {
         // the old area may still be read by work queued on this stream
         if (e.*ptr) {
@@ -137,6 +150,9 @@ bool grow_area(cudaStream_t stream, size_t bytes, void *ScratchEntry::*ptr, size
 }
 
 } // namespace
+
+bool scratch_over_reservation() { return t_over_reservation; }
+void clear_scratch_over_reservation() { t_over_reservation = false; }
 
 bool get_w16_scratch(cudaStream_t stream, size_t bytes, void **out)
 {
@@ -182,6 +198,18 @@ using awq::Problem;
 namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Status of a call whose launches returned `e`: a scratch need beyond the
+// stream's reservation is AWQ_ERR_TOO_LARGE, any other failure AWQ_ERR_CUDA.
+awq_status_t launch_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return AWQ_OK;
+    if (awq::scratch_over_reservation()) {
+        awq::clear_scratch_over_reservation();
+        return AWQ_ERR_TOO_LARGE;
+    }
+    return AWQ_ERR_CUDA;
+}
 
 // The WQLinear page's shape rules; fills the resolved group size.
 awq_status_t check_shape(int64_t K, int64_t N, int64_t group_size, int64_t *g_out)
@@ -323,7 +351,7 @@ awq_status_t awq_linear_forward_path(const void *x, const int32_t *qweight, cons
     case AWQ_PATH_DEQUANT_GEMM: e = awq::launch_dequant_gemm(p, s); break;
     default: e = awq::launch_generic(p, s); break;
     }
-    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+    return launch_status(e);
 }
 
 awq_status_t awq_linear_forward(const void *x, const int32_t *qweight, const int32_t *qzeros,
@@ -345,7 +373,7 @@ awq_status_t awq_dequant(const int32_t *qweight, const int32_t *qzeros, const vo
         return AWQ_ERR_MISALIGNED;
     Problem p{nullptr, qweight, qzeros, scales, nullptr, nullptr, 0, K, N, g, K / g};
     cudaError_t e = awq::launch_dequant(p, W, reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+    return launch_status(e);
 }
 
 awq_status_t awq_linear_forward_rows(const void *x, int64_t ldx, const int32_t *qweight,
@@ -374,7 +402,7 @@ awq_status_t awq_linear_forward_rows(const void *x, int64_t ldx, const int32_t *
     case AWQ_PATH_DEQUANT_GEMM: e = awq::launch_dequant_gemm(p, s); break;
     default: e = awq::launch_generic(p, s); break;
     }
-    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+    return launch_status(e);
 }
 
 awq_status_t awq_finish_rows(const float *y32, const void *bias, void *y, int64_t M, int64_t N,
@@ -385,7 +413,7 @@ awq_status_t awq_finish_rows(const float *y32, const void *bias, void *y, int64_
     if (!y32 || !y) return AWQ_ERR_INVALID_ARG;
     if (!aligned16(y32) || !aligned16(y) || (bias && !aligned16(bias))) return AWQ_ERR_MISALIGNED;
     cudaError_t e = awq::launch_finish_rows(y32, bias, y, M, N, reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+    return launch_status(e);
 }
 
 awq_status_t awq_dequant_gidx(const int32_t *qweight, const int32_t *qzeros, const void *scales,
@@ -399,7 +427,7 @@ awq_status_t awq_dequant_gidx(const int32_t *qweight, const int32_t *qzeros, con
         return AWQ_ERR_MISALIGNED;
     Problem p{nullptr, qweight, qzeros, scales, nullptr, nullptr, 0, K, N, 0, G};
     cudaError_t e = awq::launch_dequant_gidx(p, g_idx, W, reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+    return launch_status(e);
 }
 
 awq_status_t awq_linear_forward_gidx(const void *x, const int32_t *qweight, const int32_t *qzeros,
@@ -416,14 +444,14 @@ awq_status_t awq_linear_forward_gidx(const void *x, const int32_t *qweight, cons
         return AWQ_ERR_MISALIGNED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     void *w16 = nullptr;
-    if (!awq::get_w16_scratch(s, (size_t)K * (size_t)N * 2, &w16)) return AWQ_ERR_CUDA;
+    if (!awq::get_w16_scratch(s, (size_t)K * (size_t)N * 2, &w16)) return launch_status(cudaErrorMemoryAllocation);
     Problem pw{nullptr, qweight, qzeros, scales, nullptr, nullptr, 0, K, N, 0, G};
     cudaError_t e = awq::launch_dequant_gidx(pw, g_idx, w16, s);
     if (e == cudaSuccess) {
         Problem pg{x, nullptr, nullptr, nullptr, bias, y, M, K, N, K, 1};
         e = awq::launch_gemm_f16(pg, w16, s);
     }
-    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+    return launch_status(e);
 }
 
 awq_status_t awq_gidx_sort(const int32_t *g_idx, int64_t K, int64_t G, int32_t *perm)
@@ -452,7 +480,7 @@ awq_status_t awq_permute_rows(const int32_t *qweight, const int32_t *perm, int32
     if (!aligned16(qweight) || !aligned16(perm) || !aligned16(qweight_sorted)) return AWQ_ERR_MISALIGNED;
     cudaError_t e = awq::launch_gather_rows(qweight, perm, qweight_sorted, K, N / 8,
                                             reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+    return launch_status(e);
 }
 
 awq_status_t awq_linear_forward_sorted(const void *x, const int32_t *perm, const int32_t *qweight_sorted,
@@ -476,10 +504,10 @@ awq_status_t awq_linear_forward_sorted(const void *x, const int32_t *perm, const
         // the weights are dequantised anyway: put their rows back in the
         // original order while doing so, and leave x as it is
         p.row_perm = perm;
-        return awq::launch_dequant_gemm(p, s) == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+        return launch_status(awq::launch_dequant_gemm(p, s));
     }
     void *xs = nullptr;
-    if (!awq::get_xs_scratch(s, (size_t)M * (size_t)K * 2, &xs)) return AWQ_ERR_CUDA;
+    if (!awq::get_xs_scratch(s, (size_t)M * (size_t)K * 2, &xs)) return launch_status(cudaErrorMemoryAllocation);
     if (awq::launch_gather_cols(x, K, perm, xs, M, K, s) != cudaSuccess) return AWQ_ERR_CUDA;
     return awq_linear_forward_path(xs, qweight_sorted, qzeros, scales, bias, y, M, K, N, group_size, stream,
                                    AWQ_PATH_AUTO);
@@ -493,7 +521,7 @@ awq_status_t awq_pack(const uint8_t *codes, int32_t *packed, int64_t rows, int64
     if (!codes || !packed) return AWQ_ERR_INVALID_ARG;
     if (!aligned16(codes) || !aligned16(packed)) return AWQ_ERR_MISALIGNED;
     cudaError_t e = awq::launch_pack(codes, packed, rows, cols, reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+    return launch_status(e);
 }
 
 awq_status_t awq_quantize_rtn(const void *W, const void *scales, const int32_t *qzeros,
@@ -508,7 +536,7 @@ awq_status_t awq_quantize_rtn(const void *W, const void *scales, const int32_t *
         return AWQ_ERR_MISALIGNED;
     Problem p{nullptr, nullptr, qzeros, scales, nullptr, nullptr, 0, K, N, g, K / g};
     cudaError_t e = awq::launch_quantize(p, W, qweight, reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+    return launch_status(e);
 }
 
 awq_status_t awq_gemm_f16(const void *x, const void *W, const void *bias, void *y, int64_t M,
@@ -522,7 +550,52 @@ awq_status_t awq_gemm_f16(const void *x, const void *W, const void *bias, void *
         return AWQ_ERR_MISALIGNED;
     Problem p{x, nullptr, nullptr, nullptr, bias, y, M, K, N, K, 1};
     cudaError_t e = awq::launch_gemm_f16(p, W, reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
+    return launch_status(e);
+}
+
+awq_status_t awq_reserve(int64_t max_M, int64_t max_K, int64_t max_N, unsigned flags, awq_stream_t stream)
+{
+    if (max_M < 0 || max_K <= 0 || max_N <= 0 || (flags & ~3u) != 0) return AWQ_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return AWQ_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    {
+        // a stream reserved before may be reserved again (larger): lift the
+        // lock for the growth below
+        std::lock_guard<std::mutex> lock(awq::g_mutex);
+        awq::g_scratch[std::make_pair(dev, s)].reserved = false;
+    }
+    const size_t partials = std::max(awq::decode_partial_floats_max(sms), awq::prefill_partial_floats_max(sms));
+    const size_t tiles = (size_t)((max_N + 255) / 256);
+    awq::Scratch sc{};
+    bool ok = awq::get_scratch(s, partials, tiles, &sc);
+    void *area = nullptr;
+    if (ok && max_M >= kDequantGemmMinM) {
+        // dequantise-then-GEMM windows: K x (a multiple of 256 columns within
+        // 256 MiB of fp16, or all of N), for every K up to max_K
+        const size_t window = (size_t)max_K * (size_t)awq::dequant_gemm_window(max_K, max_N) * 2;
+        const size_t bound = std::min((size_t)max_K * (size_t)max_N * 2,
+                                      std::max((size_t)256 << 20, (size_t)512 * (size_t)max_K));
+        ok = awq::get_w16_scratch(s, std::max(window, bound), &area);
+    }
+    if (ok && (flags & AWQ_RESERVE_GIDX)) {
+        size_t need = (size_t)max_K * (size_t)max_N * 2;   // the whole layer, dequantised
+        size_t have = 0;
+        {
+            std::lock_guard<std::mutex> lock(awq::g_mutex);
+            have = awq::g_scratch[std::make_pair(dev, s)].w16_bytes;
+        }
+        ok = awq::get_w16_scratch(s, std::max(need, have), &area);
+    }
+    if (ok && (flags & AWQ_RESERVE_SORTED)) ok = awq::get_xs_scratch(s, (size_t)max_M * (size_t)max_K * 2, &area);
+    if (!ok) return AWQ_ERR_CUDA;
+    // growth above may have queued zeroing work: let it finish, then pin
+    if (cudaStreamSynchronize(s) != cudaSuccess) return AWQ_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(awq::g_mutex);
+    awq::g_scratch[std::make_pair(dev, s)].reserved = true;
+    return AWQ_OK;
 }
 
 awq_status_t awq_last_device_status(awq_stream_t stream)

@@ -896,6 +896,8 @@ bool decode_supported(int64_t M, int64_t K, int64_t N, int64_t g)
                (int64_t(1) << 30);
 }
 
+size_t decode_partial_floats_max(int sms) { return (size_t)2 * (size_t)sms * kMaxPartialFloats; }
+
 int decode_tile_columns(int64_t M, int64_t K, int64_t N, int64_t g)
 {
     if (!decode_supported(M, K, N, g)) return 0;

@@ -53,8 +53,17 @@ constexpr unsigned int kStatusTimeout = 1u;
 constexpr unsigned int kStatusBadIndex = 2u;   // a group or row index out of range
 
 // Scratch for `stream` on the current device, grown to at least the given
-// sizes. Returns false if an allocation failed.
+// sizes. Returns false if an allocation failed, or if the stream's scratch
+// was reserved (awq_reserve) and is smaller than asked: a reserved area never
+// grows (scratch_over_reservation() then reports true on this thread).
 bool get_scratch(cudaStream_t stream, size_t partial_floats, size_t n_counters, Scratch *out);
+bool scratch_over_reservation();
+void clear_scratch_over_reservation();
+
+// Largest split-K partial areas (floats) a decode / prefill launch on a GPU
+// with `sms` SMs asks for, whatever the shape.
+size_t decode_partial_floats_max(int sms);
+size_t prefill_partial_floats_max(int sms);
 
 // A buffer of at least `bytes` for `stream` on the current device (dequantised
 // weights of the g_idx forward), grown on demand.

@@ -895,6 +895,10 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int6
 
 } // namespace
 
+// every stream-K CTA (at most one per SM) keeps two pieces of up to two
+// 128-row halves
+size_t prefill_partial_floats_max(int sms) { return (size_t)2 * (size_t)sms * 2 * kPartialFloats; }
+
 bool prefill_supported(int64_t M, int64_t K, int64_t N, int64_t g)
 {
     return M >= 1 && M < (int64_t(1) << 31) && K % 16 == 0 && N % 32 == 0 && g % 16 == 0 &&

@@ -38,13 +38,15 @@
  *     Argument errors are returned before anything is enqueued. A device-side
  *     error (a bounded wait that timed out) is recorded in a per-device status
  *     word that awq_last_device_status() reads.
- *   - The library keeps, per (device, stream), a lazily created scratch area
- *     for split-K partial sums (allocated with cudaMalloc on first use on that
- *     stream, freed by awq_shutdown). An area that has to grow for a larger
- *     need (a prefill-sized call after decode-sized ones, say) is replaced
- *     after a cudaStreamSynchronize of that stream, which a stream capture
- *     does not allow: before capturing a stream into a CUDA graph, make on it
- *     one call of every shape and path the graph will hold.
+ *   - The library keeps, per (device, stream), a scratch area for split-K
+ *     partial sums (and, on some paths, dequantised weights or reordered
+ *     activations), freed by awq_shutdown. Either reserve it up front with
+ *     awq_reserve() -- then no call on that stream allocates or synchronises,
+ *     and a call that would need more returns AWQ_ERR_TOO_LARGE -- or let it
+ *     grow lazily: the first call that needs more than the stream holds
+ *     synchronises the stream and replaces the area (cudaFree + cudaMalloc),
+ *     which a stream capture does not allow, so make one call of every shape
+ *     and path on the stream before capturing it into a CUDA graph.
  *   - Thread safety: calls may come from several host threads on different
  *     streams. Two host threads must not call at the same time on one stream
  *     (a growing scratch area could be freed under the other call).
@@ -69,7 +71,8 @@ typedef enum {
     AWQ_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed */
     AWQ_ERR_TIMEOUT = 4,     /* a kernel's bounded wait ran out (device status only) */
     AWQ_ERR_TOO_LARGE = 5    /* the shape needs more than the fixed scratch of
-                                awq_linear_forward_decode_noalloc */
+                                awq_linear_forward_decode_noalloc, or more than
+                                the stream's reservation (awq_reserve) */
 } awq_status_t;
 
 /* Which kernel family serves a forward call. */
@@ -344,6 +347,38 @@ awq_status_t awq_linear_forward_decode_noalloc(const void *x, const int32_t *qwe
                                                const void *bias, void *y, int64_t M,
                                                int64_t K, int64_t N, int64_t group_size,
                                                awq_stream_t stream);
+
+/*
+ * awq_reserve -- sizes, once, every scratch area the library keeps for
+ * `stream` on the current device, so that later calls on that stream never
+ * allocate and never synchronise. Without it the areas are created and grown
+ * lazily: a call that needs more than its stream holds synchronises the
+ * stream, frees the old area and allocates a larger one.
+ *
+ *   max_M, max_K, max_N  the largest M, K and N the stream's calls will use
+ *                        (max_M >= 0, max_K > 0, max_N > 0)
+ *   flags                0, or-ed with AWQ_RESERVE_SORTED (room for x's
+ *                        columns in sorted order, max_M x max_K fp16:
+ *                        awq_linear_forward_sorted) and AWQ_RESERVE_GIDX
+ *                        (room for a whole dequantised layer, max_K x max_N
+ *                        fp16: awq_linear_forward_gidx)
+ *
+ * It reserves the split-K partials of the decode and prefill kernels (sized
+ * for the GPU's SM count, whatever the shape), the arrival counters of up to
+ * ceil(max_N / 256) column tiles and, when max_M reaches the
+ * dequantise-then-GEMM crossover (M >= 6144), that path's fp16 weight window.
+ * This call itself allocates and synchronises `stream`: make it at set-up,
+ * before any stream capture. Afterwards the stream's areas are fixed: a
+ * forward call (any path) that would need more returns AWQ_ERR_TOO_LARGE
+ * before launching anything, instead of growing them. Calling awq_reserve
+ * again with larger bounds grows the areas; awq_shutdown() drops every
+ * reservation. Returns AWQ_ERR_INVALID_ARG for invalid bounds or flags,
+ * AWQ_ERR_CUDA if an allocation failed.
+ */
+#define AWQ_RESERVE_SORTED 1u
+#define AWQ_RESERVE_GIDX 2u
+awq_status_t awq_reserve(int64_t max_M, int64_t max_K, int64_t max_N, unsigned flags,
+                         awq_stream_t stream);
 
 /* Static description of a status code. Never NULL. */
 const char *awq_status_string(awq_status_t status);

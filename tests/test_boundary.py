@@ -251,3 +251,10 @@ def test_fault_test_build_exports_the_switch_and_the_main_library_does_not(lib):
     assert re.search(r"\sT\sawq_test_inject_fault\b", ft)
     for n in awq.EXPORTED:
         assert re.search(rf"\sT\s{n}\b", ft), n
+
+
+@pytest.mark.parametrize("args", [(-1, 4096, 4096, 0), (1, 0, 4096, 0), (1, 4096, 0, 0), (1, 4096, 4096, 4),
+                                  (1, 4096, 4096, 0xFFFFFFFF)])
+def test_reserve_invalid_args(lib, args):
+    """awq_reserve checks its bounds and flags before any CUDA call."""
+    assert awq.awq_reserve(*args, None) == Status.ERR_INVALID_ARG
