@@ -10,6 +10,8 @@ wrapper (``layer``) and a seeded input generator (``synthetic``).
 from ._binding import (  # noqa: F401
     EXPORTED,
     LIB_PATH,
+    RESERVE_GIDX,
+    RESERVE_SORTED,
     AWQError,
     Path,
     Status,

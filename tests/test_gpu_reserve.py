@@ -82,9 +82,11 @@ def test_call_beyond_the_reservation_is_refused(gpu):
     h = stream.cuda_stream
     assert awq.awq_reserve(16, 4096, 4096, 0, h) == Status.OK
     small = make_problem(4, 4096, 4096, 128, bias=False, seed=3).to("cuda")
-    wide = make_problem(4, 4096, 8192, 128, bias=False, seed=4).to("cuda")   # more column tiles
+    # 127 column tiles: more arrival counters than the reservation holds (it
+    # keeps headroom above the 16 tiles asked for, but not that much)
+    wide = make_problem(4, 4096, 32512, 128, bias=False, seed=4).to("cuda")
     y_small = torch.empty((4, 4096), dtype=torch.float16, device="cuda")
-    y_wide = torch.empty((4, 8192), dtype=torch.float16, device="cuda")
+    y_wide = torch.empty((4, 32512), dtype=torch.float16, device="cuda")
     assert _fwd(wide, y_wide, h) == Status.ERR_TOO_LARGE
     # the sorted forward's reorder area was not reserved
     assert awq.awq_linear_forward_sorted(small.x.data_ptr(), small.qweight.data_ptr(), small.qweight.data_ptr(),
@@ -96,6 +98,6 @@ def test_call_beyond_the_reservation_is_refused(gpu):
     cpu = make_problem(4, 4096, 4096, 128, bias=False, seed=3)
     assert_close(y_small.cpu().numpy(), oracle_reference(cpu), "within the reservation")
     # a larger reservation lifts the limit
-    assert awq.awq_reserve(16, 4096, 8192, 0, h) == Status.OK
+    assert awq.awq_reserve(16, 4096, 32512, 0, h) == Status.OK
     assert _fwd(wide, y_wide, h) == Status.OK
     assert awq.awq_last_device_status(h) == Status.OK
