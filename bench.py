@@ -59,7 +59,35 @@ METRIC = "AWQ W4A16 GEMM TFLOP/s and weight GB/s vs M (1..8192), % of roofline, 
 # workload (dram__bytes_read.sum + dram__bytes_write.sum, mean over one step's
 # launches of the family), valid only while the kernel sources hash to what
 # was captured. Keys: (workload, family).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # (workload, family) -> mean DRAM read + write per launch (decode) or per
+    # call (tcgen05: the call's launches summed) from one ncu capture of the
+    # first eager pass, valid while the kernel sources hash as below
+    ("full", "decode"): {
+        "bytes_per_launch": 95164800,
+        "sources": {
+            "bit_weight_quantized_awq_gb300/csrc/awq_decode.cu":
+                "d6cc70b52a151674641b6811a6f6945618b125f27feeed1bd010717ad2b2dc78",
+            "bit_weight_quantized_awq_gb300/csrc/awq_device.cuh":
+                "4b1e014a6cc0d4d37d2f75930f7d0d219070cc433d551fa9957cbdd2f737ce58",
+        },
+        "summary": "profiles/full_step_launches_and_traffic.md (30 decode launches of one pass)",
+    },
+    ("full", "tcgen05"): {
+        "bytes_per_launch": 810837484,
+        "sources": {
+            "bit_weight_quantized_awq_gb300/csrc/awq_prefill.cu":
+                "611d7f8a67e9840e735046ba09db83e24fc49ad17631e30985fd634ba20261a5",
+            "bit_weight_quantized_awq_gb300/csrc/awq_tcgen05.cuh":
+                "7583bdc482c3f999df48aafe74db217e2c2055ec6f41779622d85db462730d4a",
+            "bit_weight_quantized_awq_gb300/csrc/awq_dequant.cu":
+                "8062f0eddd6c436eb4452f43d9a64097041ee680fec5a9281620994bd0f23bdf",
+            "bit_weight_quantized_awq_gb300/csrc/awq_device.cuh":
+                "4b1e014a6cc0d4d37d2f75930f7d0d219070cc433d551fa9957cbdd2f737ce58",
+        },
+        "summary": "profiles/full_step_launches_and_traffic.md (25 calls of one pass, per call)",
+    },
+}
 
 
 def ncu_traffic(workload, family):
