@@ -259,7 +259,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             };
             auto issue_x = [&](int sl, int kbx) {
                 ptx::tma_load_3d(ptx::smem_addr(smem + (uint32_t)sl * SB + p.x_off), &tm_x,
-                                 ptx::smem_addr(full + sl), 0, kbx * kKBlocks, 0);
+                                 ptx::smem_addr(full + sl), 0, 0, kbx * kKBlocks);
             };
             auto advance = [&]() {
                 if (++kb == p.kiters) { kb = 0; ++tile; }
@@ -335,20 +335,22 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     const uint32_t offB = rowbase + qB * 128 + ((unit ^ (qB & 7)) << 4) + inw;
     constexpr uint32_t kChunkStride = 16 * CW * 128;   // 16 rows
     constexpr uint32_t kRow8 = 8 * CW * 128;           // 8 rows
-    // activation slice: [token m][64-row block][64 halves], 128-byte rows
-    // (r = m * kKBlocks + block), 16-byte unit u of row r stored at unit
+    // activation slice: [64-row block][token m][64 halves], 128-byte rows
+    // (r = block * 8 MT + m), 16-byte unit u of row r stored at unit
     // u ^ (r % 8). Chunk j of this warp is block R0 / 64 + j / 4, units
     // 2 (j % 4) and 2 (j % 4) + 1 -- the k 0..7 and 8..15 halves of its B
     // operand. One ldmatrix.x4 fetches the B operands of a chunk pair for
-    // eight tokens: lane L addresses token L % 8, unit 4 * pair + L / 8.
-    // Token tile mt adds 8 kKBlocks rows, which keeps r % 8.
+    // eight tokens: lane L addresses token L % 8, unit 4 * pair + L / 8. The
+    // eight rows of one 8 x 8 matrix are eight consecutive tokens, so r % 8
+    // takes every value once and the eight 16-byte reads fall in distinct
+    // banks. Token tile mt adds 8 rows, which keeps r % 8.
     constexpr int kBlocksPerWarp = kChunksPerWarp / 4;
     static_assert(kChunksPerWarp % 4 == 0, "whole 64-row activation blocks per warp and stage");
-    constexpr uint32_t kXTokenTile = 8 * kKBlocks * 128;
+    constexpr uint32_t kXTokenTile = 8 * 128;
     uint32_t xoff[kBlocksPerWarp][2];
 #pragma unroll
     for (int jb = 0; jb < kBlocksPerWarp; ++jb) {
-        const uint32_t r = (uint32_t)((lane & 7) * kKBlocks + R0 / 64 + jb);
+        const uint32_t r = (uint32_t)((R0 / 64 + jb) * (8 * MT) + (lane & 7));
 #pragma unroll
         for (int pr = 0; pr < 2; ++pr)
             xoff[jb][pr] = p.x_off + r * 128 + (((uint32_t)(4 * pr + (lane >> 3)) ^ (r & 7)) << 4);
@@ -728,10 +730,12 @@ bool build_maps(const Problem &pr, int mpad, CUtensorMap *tw, CUtensorMap *tx, C
     using G = Geo<CW>;
     const uint64_t K = (uint64_t)pr.K, N = (uint64_t)pr.N, M = (uint64_t)pr.M, Gn = (uint64_t)pr.G;
     const int R = group_rows_per_stage(pr.g, G::kStageRows);
-    // x viewed as [M][K / 64][64]: one box covers a stage's k for every token
+    // x viewed as [K / 64][M][64] (a 64-column block of every token, block
+    // by block): one box covers a stage's k for every token, stored block
+    // by block in shared memory
     const uint64_t ldx = pr.ldx > 0 ? (uint64_t)pr.ldx : K;
-    const uint64_t xd[3] = {64, K / 64, M}, xs[2] = {128, ldx * 2};
-    const uint32_t xb[3] = {64, (uint32_t)G::kKBlocks, (uint32_t)mpad};
+    const uint64_t xd[3] = {64, M, K / 64}, xs[2] = {ldx * 2, 128};
+    const uint32_t xb[3] = {64, (uint32_t)mpad, (uint32_t)G::kKBlocks};
     bool ok = make_map(tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.x, 3, xd, xs, xb, CU_TENSOR_MAP_SWIZZLE_128B);
     if (CW == 1) {
         const uint64_t wd[2] = {N / 8, K}, ws[1] = {N / 2};

@@ -50,6 +50,7 @@
 // Requirements (else another path serves): K % 16 == 0, N % 32 == 0,
 // group_size % 16 == 0, base pointers 16-byte aligned.
 #include <algorithm>
+#include <cstring>
 #include <map>
 #include <mutex>
 
@@ -70,6 +71,7 @@ constexpr int kMmaK = 16;
 constexpr int kMaxGroupRows = 5;
 
 constexpr int kABytes = BM * BK * 2;            // 16 KB
+constexpr int kEpiWarpBytes = 32 * 128;         // 32 rows x 64 fp16 columns of output
 constexpr int kBBytes = BN * BK * 2;            // 32 KB
 constexpr int kPBytes = BK * (BN / 8) * 4;      // 8 KB
 
@@ -95,10 +97,12 @@ struct Cfg {
     static constexpr int kStageBytes = kDequant ? (MH == 1 ? 28 : 44) * 1024 : kATile + kBBytes;
     static constexpr int kBSlots = kDequant ? 2 : 0;
     static constexpr int kBSlotOff = kStages * kStageBytes;
-    static constexpr int kBarOff = kBSlotOff + kBSlots * kBBytes;
+    static constexpr int kEpiOff = kBSlotOff + kBSlots * kBBytes;   // epilogue staging, 4 KB per warp
+    static constexpr int kBarOff = kEpiOff + 4 * kEpiWarpBytes;
     static constexpr int kSmemBytes = kBarOff + 256 + 1024;
     static_assert(!kDequant || kZOff + kMaxGroupRows * (BN / 8) * 4 <= kStageBytes, "stage layout overflows");
-    static_assert(kStageBytes % 1024 == 0 && kBSlotOff % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+    static_assert(kStageBytes % 1024 == 0 && kBSlotOff % 1024 == 0 && kEpiOff % 1024 == 0,
+                  "swizzled tiles need 1024-byte alignment");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -254,7 +258,7 @@ template <bool kDequant, bool kWhole, int MH>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
-               const PrefillParams p)
+               const __grid_constant__ CUtensorMap tm_y, const PrefillParams p)
 {
     using C = Cfg<kDequant, MH>;
     constexpr int kStages = C::kStages;
@@ -523,18 +527,81 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 tc::fence_after_sync();
                 const int m = m0 + h * BM + 32 * q + lane;
                 const uint32_t t_acc = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * BN);
-                if (whole) {
-                    // ---- whole tile: + bias, one rounding, store
+                if (whole && p.y32 == nullptr) {
+                    // ---- whole tile: + bias, one rounding, staged in this
+                    //      warp's buffer (its 32 rows x 64 columns, 128-byte
+                    //      rows with the 128-byte swizzle) and written by a TMA
+                    //      store, which clips rows >= M and columns >= N
+                    const uint32_t stg = ptx::smem_addr(smem + C::kEpiOff + q * kEpiWarpBytes);
+                    const int row0 = m0 + h * BM + 32 * q;
+#pragma unroll 1
+                    for (int c2 = 0; c2 < BN / 64; ++c2) {
+                        const int col = n0 + 64 * c2;
+                        if (col >= p.N) break;
+                        // the previous store from the buffer has read it
+                        if (lane == 0) ptx::bulk_wait_read_all();
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            uint32_t raw[32];
+                            tc::ld_32x32b_x32(t_acc + (uint32_t)(64 * c2 + 32 * j), raw);
+                            tc::ld_wait();
+                            const int cj = col + 32 * j;
+                            uint32_t hv[16];
+                            if (cj < p.N) {
+                                float b[32];
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) b[e] = 0.f;
+                                if (p.bias) {
+                                    __align__(16) __half bh[32];
+#pragma unroll
+                                    for (int v = 0; v < 4; ++v)
+                                        reinterpret_cast<uint4 *>(bh)[v] =
+                                            __ldg(reinterpret_cast<const uint4 *>(p.bias + cj) + v);
+#pragma unroll
+                                    for (int e = 0; e < 32; ++e) b[e] = __half2float(bh[e]);
+                                }
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) {
+                                    const int e0 = 2 * e, e1 = 2 * e + 1;
+                                    const float v0 = __uint_as_float(kDequant ? raw[(e0 & ~7) + unperm(e0 & 7)] : raw[e0]);
+                                    const float v1 = __uint_as_float(kDequant ? raw[(e1 & ~7) + unperm(e1 & 7)] : raw[e1]);
+                                    const __half2 hh = __halves2half2(__float2half_rn(v0 + b[e0]), __float2half_rn(v1 + b[e1]));
+                                    hv[e] = *reinterpret_cast<const uint32_t *>(&hh);
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) hv[e] = 0u;
+                            }
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                const uint32_t u = (uint32_t)(4 * j + v);
+                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                                             ::"r"(stg + (uint32_t)lane * 128 + ((u ^ (uint32_t)(lane & 7)) << 4)),
+                                               "r"(hv[4 * v]), "r"(hv[4 * v + 1]), "r"(hv[4 * v + 2]), "r"(hv[4 * v + 3])
+                                             : "memory");
+                            }
+                        }
+                        // the generic-proxy writes are made visible to the TMA
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0 && row0 < p.M) {
+                            ptx::tma_store_2d(&tm_y, stg, col, row0);
+                            ptx::bulk_commit_group();
+                        }
+                    }
+                } else if (whole) {
+                    // ---- whole tile, row-shard form: y32 += the fp32 sums
 #pragma unroll 1
                     for (int c = 0; c < BN / 32; ++c) {
                         uint32_t raw[32];
                         tc::ld_32x32b_x32(t_acc + (uint32_t)(32 * c), raw);
                         tc::ld_wait();
+                        const int col = n0 + 32 * c;
                         uint32_t r[32];
 #pragma unroll
                         for (int e = 0; e < 32; ++e) r[e] = kDequant ? raw[(e & ~7) + unperm(e & 7)] : raw[e];
-                        const int col = n0 + 32 * c;
-                        if (col < p.N && m < p.M && p.y32) {
+                        if (col < p.N && m < p.M) {
                             float4 *d = reinterpret_cast<float4 *>(p.y32 + (int64_t)m * p.ldy + col);
 #pragma unroll
                             for (int v = 0; v < 8; ++v) {
@@ -545,23 +612,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                                 t.w += __uint_as_float(r[4 * v + 3]);
                                 d[v] = t;
                             }
-                        } else if (col < p.N && m < p.M) {
-                            __align__(16) __half out[32];
-                            if (p.bias) {
-                                __align__(16) __half bh[32];
-#pragma unroll
-                                for (int v = 0; v < 4; ++v)
-                                    reinterpret_cast<uint4 *>(bh)[v] = __ldg(reinterpret_cast<const uint4 *>(p.bias + col) + v);
-#pragma unroll
-                                for (int e = 0; e < 32; ++e)
-                                    out[e] = __float2half_rn(__uint_as_float(r[e]) + __half2float(bh[e]));
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 32; ++e) out[e] = __float2half_rn(__uint_as_float(r[e]));
-                            }
-                            uint4 *dst = reinterpret_cast<uint4 *>(p.y + (int64_t)m * p.ldy + col);
-#pragma unroll
-                            for (int v = 0; v < 4; ++v) dst[v] = reinterpret_cast<const uint4 *>(out)[v];
                         }
                     }
                 } else {
@@ -586,6 +636,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 ptx::mbar_arrive(ptx::smem_addr(acc_empty + ab));
             }
         }
+        // this warp's TMA stores have completed before the CTA exits
+        if (lane == 0) ptx::bulk_wait_all();
     }
     __syncthreads();
     if (warp == 1) {
@@ -844,6 +896,16 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int6
     }
     if (!ok) return cudaErrorInvalidValue;
 
+    // y for the TMA stores of whole tiles: [M, N] fp16 with row pitch ldy,
+    // boxes of 32 rows x 64 columns (not used when summing into y32)
+    CUtensorMap ty;
+    memset(&ty, 0, sizeof(ty));
+    const uint64_t ldy_eff = ldy > 0 ? (uint64_t)ldy : (uint64_t)N;
+    if (pr.y32 == nullptr &&
+        !make_map_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.y, N, M, ldy_eff * 2, 64, 32,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+
     PrefillParams p{};
     p.bias = static_cast<const __half *>(pr.bias);
     p.y = static_cast<__half *>(pr.y);
@@ -865,7 +927,7 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int6
             return cudaErrorMemoryAllocation;
         p.partials = sc.partials;
     }
-    prefill_kernel<kDequant, kWhole, MH><<<ctas, kThreads, Cfg<kDequant, MH>::kSmemBytes, stream>>>(tx, tw, ts, tz, p);
+    prefill_kernel<kDequant, kWhole, MH><<<ctas, kThreads, Cfg<kDequant, MH>::kSmemBytes, stream>>>(tx, tw, ts, tz, ty, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !split) return e;
 

@@ -152,13 +152,15 @@ def test_narrow_tile_decode(gpu, M, K, N, g, bias):
 
 
 # Prefill with fewer tiles than SMs: every tile's k-stages are split between
-# CTAs ("stream-K") and the partials summed by the last contributor. All
-# outputs are compared, and repeated runs must agree bit for bit (the sum is
-# taken in contributor order, whichever CTA performs it).
+# CTAs ("stream-K"), which leave fp32 pieces that the sum kernel adds up. All
+# outputs are compared, and repeated runs must agree bit for bit (the pieces
+# are added in contributor order).
 @pytest.mark.parametrize("M,K,N,g,bias", [
     (40, 4096, 1024, 128, True),
     (200, 2112, 800, 96, True),     # ragged tile in N, groups that split a stage
     (129, 1088, 4128, 64, False),   # two token tiles, ragged K and N
+    (512, 2112, 2080, 64, True),    # 256-row tiles, 4-5 contributors per tile (whole ranges inside a tile)
+    (300, 4224, 4128, 128, False),  # 256-row tiles, ragged M, 5-6 contributors per tile
 ])
 def test_prefill_stream_k(gpu, M, K, N, g, bias):
     p = make_problem(M, K, N, g, bias=bias, seed=M + 7)
