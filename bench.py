@@ -64,14 +64,14 @@ NCU_TRAFFIC = {
     # call (tcgen05: the call's launches summed) from one ncu capture of the
     # first eager pass, valid while the kernel sources hash as below
     ("full", "decode"): {
-        "bytes_per_launch": 95164800,
+        "bytes_per_launch": 95182626,
         "sources": {
             "bit_weight_quantized_awq_gb300/csrc/awq_decode.cu":
-                "d6cc70b52a151674641b6811a6f6945618b125f27feeed1bd010717ad2b2dc78",
+                "04892afcc1dfe943d76ab2e33aa4952a13742311b4d2a0aaa11975962480911b",
             "bit_weight_quantized_awq_gb300/csrc/awq_device.cuh":
-                "4b1e014a6cc0d4d37d2f75930f7d0d219070cc433d551fa9957cbdd2f737ce58",
+                "b046a423a76b51de6cd65483cbd97acc326bc2776db731410fa58a96f2482a61",
         },
-        "summary": "profiles/full_step_launches_and_traffic.md (30 decode launches of one pass)",
+        "summary": "profiles/decode_kernel_decode-7b.md (30 decode launches of one pass of the full workload)",
     },
     ("full", "tcgen05"): {
         "bytes_per_launch": 810837484,
