@@ -327,6 +327,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             // MMA, dequant and epilogue warps on the first stage run out
             if (p.fault && blockIdx.x == 0) ok = false;
 #endif
+            // Programmatic dependent launch: the packed weights, scales and
+            // zero points of the first stages (the ring is empty, no wait)
+            // are requested before waiting for the previous kernel; x -- and
+            // the fp16 weights of the GEMM core, which the kernel before may
+            // have written -- only after that wait.
+            int pend_k0[kStages], pend_m0[kStages];
+            int npend = 0;
+            bool waited = !kDequant;
+            if (!kDequant) ptx::wait_prerequisites();
+            auto flush_x = [&]() {
+                ptx::wait_prerequisites();
+                for (int i = 0; i < npend; ++i)
+                    ptx::tma_load_2d(ptx::smem_addr(smem + i * C::kStageBytes) + C::kAOff, &tm_x,
+                                     ptx::smem_addr(full + i), pend_k0[i], pend_m0[i]);
+                waited = true;
+            };
             for (int si = 0; si < sg.count && ok; ++si) {
                 int tile, kb0, kb1;
                 sg.get(p, si, tile, kb0, kb1);
@@ -345,7 +361,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     const uint32_t st = ptx::smem_addr(smem + s * C::kStageBytes);
                     const int k0 = kb * BK;
                     ptx::mbar_arrive_expect_tx(fb, p.stage_tx);
-                    ptx::tma_load_2d(st + C::kAOff, &tm_x, fb, k0, m0);
+                    if (waited) {
+                        ptx::tma_load_2d(st + C::kAOff, &tm_x, fb, k0, m0);
+                    } else {
+                        pend_k0[npend] = k0;   // stage npend == it
+                        pend_m0[npend] = m0;
+                        ++npend;
+                    }
                     if (kDequant) {
                         ptx::tma_load_2d(st + C::kPOff, &tm_w, fb, n0 / 8, k0);
                         ptx::tma_load_2d(st + C::kSOff, &tm_s, fb, n0, k0 / p.g);
@@ -356,8 +378,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                             ptx::tma_load_2d(st + C::kBOff + a * kBAtomStride, &tm_w, fb, n0 + 64 * a, k0);
                     }
                     issued = it + 1;
+                    if (!waited && npend == kStages) flush_x();
                 }
             }
+            if (!waited) flush_x();
             if (!ok) {
                 // let the copies already in flight land before the CTA exits
                 for (int i = std::max(0, issued - kStages); i < issued; ++i)
@@ -498,6 +522,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        // bias, y and the stream-K scratch may be in use by the previous
+        // kernel until it completes
+        ptx::wait_prerequisites();
         const int q = warp & 3;                 // TMEM lane quarter this warp may read
         int acc_it = 0;
         bool ok = true;
@@ -669,6 +696,9 @@ template <bool kDequant, int MH>
 __global__ void __launch_bounds__(BM)
 sk_fixup_kernel(const FixupParams p)
 {
+    // the next kernel may be scheduled now (it waits for this grid, which
+    // itself has waited for the main grid)
+    ptx::launch_dependents();
     ptx::wait_prerequisites();
     const int t = blockIdx.x / (MH * (BN / 32));
     const int h = (blockIdx.x / (BN / 32)) % MH;
@@ -927,8 +957,20 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int6
             return cudaErrorMemoryAllocation;
         p.partials = sc.partials;
     }
-    prefill_kernel<kDequant, kWhole, MH><<<ctas, kThreads, Cfg<kDequant, MH>::kSmemBytes, stream>>>(tx, tw, ts, tz, ty, p);
-    cudaError_t e = cudaGetLastError();
+    // programmatic dependent launch: the CTAs may start while the previous
+    // kernel drains (they wait for it before touching what it writes)
+    cudaLaunchConfig_t mcfg{};
+    mcfg.gridDim = dim3((unsigned)ctas);
+    mcfg.blockDim = dim3(kThreads);
+    mcfg.dynamicSmemBytes = Cfg<kDequant, MH>::kSmemBytes;
+    mcfg.stream = stream;
+    cudaLaunchAttribute mattr[1];
+    mattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    mattr[0].val.programmaticStreamSerializationAllowed = 1;
+    mcfg.attrs = mattr;
+    mcfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&mcfg, prefill_kernel<kDequant, kWhole, MH>, tx, tw, ts, tz, ty, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess || !split) return e;
 
     FixupParams f{};

@@ -342,10 +342,7 @@ def test_library_cross_check_cublas(gpu):
 # bit, the same calls with a device synchronisation after each.
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("M", [1, 16])
-@pytest.mark.parametrize("path", [Path.DECODE, Path.AUTO])
-@pytest.mark.parametrize("KN", [2048, 8192])
-def test_chained_layers_match_serialised(gpu, M, path, KN):
+def _chain_matches_serialised(M, path, KN):
     K = N = KN
     layers = [make_problem(M, K, N, 128, bias=(i == 1), seed=40 + i).to(torch.device("cuda"))
               for i in range(4)]
@@ -373,3 +370,22 @@ def test_chained_layers_match_serialised(gpu, M, path, KN):
                          p0.scales.cpu().numpy(), None, p0.group_size)
     assert_close(serial[0].cpu().numpy(), ref, "chained layer 0")
     assert awq_last_device_status(torch.cuda.current_stream().cuda_stream) == 0
+
+
+@pytest.mark.parametrize("M", [1, 16])
+@pytest.mark.parametrize("path", [Path.DECODE, Path.AUTO])
+@pytest.mark.parametrize("KN", [2048, 8192])
+def test_chained_layers_match_serialised(gpu, M, path, KN):
+    _chain_matches_serialised(M, path, KN)
+
+
+# The same chain on the tensor-core paths, which are launched as programmatic
+# dependents too: the fused kernel requests its first stages' packed weights
+# before waiting for the previous kernel, x and everything it writes after;
+# the stream-K sum kernel lets the next layer's kernel be scheduled early.
+# M = 512 at K = N = 2048 splits every tile along k (sum kernel in the
+# chain); M = 2560 at K = N = 4096 has a whole wave and a split last wave.
+@pytest.mark.parametrize("M,KN", [(512, 2048), (2560, 4096)])
+@pytest.mark.parametrize("path", [Path.PREFILL, Path.DEQUANT_GEMM])
+def test_chained_prefill_layers_match_serialised(gpu, M, KN, path):
+    _chain_matches_serialised(M, path, KN)
