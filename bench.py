@@ -74,16 +74,16 @@ NCU_TRAFFIC = {
         "summary": "profiles/decode_kernel_decode-7b.md (30 decode launches of one pass of the full workload)",
     },
     ("full", "tcgen05"): {
-        "bytes_per_launch": 810837484,
+        "bytes_per_launch": 823374070,
         "sources": {
             "bit_weight_quantized_awq_gb300/csrc/awq_prefill.cu":
-                "611d7f8a67e9840e735046ba09db83e24fc49ad17631e30985fd634ba20261a5",
+                "c1728e529d832dfbcc93de185f6b0f342d7ff2a27b2d325d3adfa7ae1e08710d",
             "bit_weight_quantized_awq_gb300/csrc/awq_tcgen05.cuh":
                 "7583bdc482c3f999df48aafe74db217e2c2055ec6f41779622d85db462730d4a",
             "bit_weight_quantized_awq_gb300/csrc/awq_dequant.cu":
                 "8062f0eddd6c436eb4452f43d9a64097041ee680fec5a9281620994bd0f23bdf",
             "bit_weight_quantized_awq_gb300/csrc/awq_device.cuh":
-                "4b1e014a6cc0d4d37d2f75930f7d0d219070cc433d551fa9957cbdd2f737ce58",
+                "b046a423a76b51de6cd65483cbd97acc326bc2776db731410fa58a96f2482a61",
         },
         "summary": "profiles/full_step_launches_and_traffic.md (25 calls of one pass, per call)",
     },
