@@ -812,7 +812,8 @@ int group_rows_per_stage(int64_t g)
 // over for a last, partial wave are split along k ("stream-K") between up to
 // one CTA per SM, each taking at least kMinUnits k-stages, so that the last
 // wave keeps every SM busy instead of a few; sk_fixup_kernel then sums the
-// pieces of every tile that was split.
+// pieces of every tile that was split. Where that wave already fills most
+// SMs, it runs whole instead (split_last_wave).
 struct Plan {
     int tiles_m, tiles_n, kiters;
     int group_m;
@@ -843,7 +844,7 @@ int group_rows(int tiles_m, int tiles_n, int64_t K, int sms, int mh)
     return (int)gm;
 }
 
-Plan plan_tiles(int64_t M, int64_t K, int64_t N, int sms, int mh)
+Plan plan_tiles(int64_t M, int64_t K, int64_t N, int sms, int mh, bool allow_split)
 {
     constexpr int kMinUnits = 8;
     Plan pl{};
@@ -855,12 +856,31 @@ Plan plan_tiles(int64_t M, int64_t K, int64_t N, int sms, int mh)
     pl.dp_waves = (int)(n_tiles / sms);
     pl.sk_tiles = (int)(n_tiles - (int64_t)pl.dp_waves * sms);
     const int64_t sk_units = (int64_t)pl.sk_tiles * pl.kiters;
+    // without splitting, the last wave's tiles go whole to one CTA each
     pl.sk_ctas = pl.sk_tiles == 0 ? 0
+                 : !allow_split ? pl.sk_tiles
                  : (int)std::min<int64_t>(sms, std::max<int64_t>(pl.sk_tiles, sk_units / kMinUnits));
     pl.ctas = pl.dp_waves > 0 ? sms : pl.sk_ctas;
     pl.split = pl.sk_tiles > 0 && pl.sk_ctas > pl.sk_tiles;
     pl.ok = sk_units < (int64_t(1) << 31);
     return pl;
+}
+
+// Whether to split the last, partial wave of tiles along k. Splitting
+// spreads its k-stages over every SM but costs the sum kernel, which reads
+// every piece back (about 0.05 us per 256 KB piece, plus 3 us); leaving the
+// wave whole costs one tile's time with SMs idle. Estimates in microseconds,
+// from a sweep of both choices over M = 512..8192 and the 7B and 70B
+// projection shapes: a 256 x 256 x 64 stage takes about 0.8 us.
+bool split_last_wave(int64_t M, int64_t K, int64_t N, int sms, int mh)
+{
+    const Plan pl = plan_tiles(M, K, N, sms, mh, true);
+    if (!pl.split || mh != 2) return true;
+    const double kStageUs = 0.8, kPieceUs = 0.052, kSumUs = 3.0;
+    const double tile_us = (double)pl.kiters * kStageUs;
+    const double split_us = (double)pl.sk_tiles / (double)sms * tile_us +
+                            (double)(pl.sk_ctas + pl.sk_tiles) * kPieceUs + kSumUs;
+    return split_us <= tile_us;
 }
 
 struct LaunchInfo {
@@ -897,7 +917,7 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int6
     const LaunchInfo li = launch_info<kDequant, kWhole, MH>();
     if (li.err != cudaSuccess) return li.err;
     const int M = (int)pr.M, K = (int)pr.K, N = (int)pr.N, g = (int)pr.g;
-    const Plan pl = plan_tiles(M, K, N, li.sms, MH);
+    const Plan pl = plan_tiles(M, K, N, li.sms, MH, split_last_wave(M, K, N, li.sms, MH));
     if (!pl.ok) return cudaErrorInvalidValue;
     const int tiles_m = pl.tiles_m, tiles_n = pl.tiles_n, kiters = pl.kiters;
     const int dp_waves = pl.dp_waves, sk_tiles = pl.sk_tiles, sk_ctas = pl.sk_ctas, ctas = pl.ctas;
@@ -1035,7 +1055,8 @@ cudaError_t launch_gemm_f16(const Problem &p, const void *w16, cudaStream_t stre
 
 int prefill_launches(int64_t M, int64_t K, int64_t N, int sms)
 {
-    return plan_tiles(M, K, N, sms, m_halves(M)).split ? 2 : 1;
+    const int mh = m_halves(M);
+    return plan_tiles(M, K, N, sms, mh, split_last_wave(M, K, N, sms, mh)).split ? 2 : 1;
 }
 
 } // namespace awq

@@ -171,6 +171,18 @@ def test_prefill_stream_k(gpu, M, K, N, g, bias):
         assert torch.equal(run_path(pg, Path.PREFILL).view(torch.int16), y0.view(torch.int16))
 
 
+# A last, partial wave that fills most SMs runs whole: one tile per CTA, no
+# pieces, no sum kernel (the tile width stays 256 columns; at 152 SMs this
+# shape has 130 tiles of 10 k-stages, where splitting would cost more than
+# the idle SMs). Groups of 64 split every 64-row stage in two.
+def test_last_wave_whole(gpu):
+    p = make_problem(384, 640, 16640, 64, bias=True, seed=384)
+    check_problem(p, paths=[Path.PREFILL], full=False)
+    pg = p.to("cuda")
+    y0 = run_path(pg, Path.PREFILL)
+    assert torch.equal(run_path(pg, Path.PREFILL).view(torch.int16), y0.view(torch.int16))
+
+
 # x larger than the L2 share the tile order plans for, on the fused kernel
 # and on the GEMM core; sampled rows and column blocks:
 #  * K = 4096, N = 2560: 18 row blocks of 256 in bands of 16 (the share
