@@ -437,10 +437,15 @@ def run_native(args, problems, device):
 
 
 def run_e2e(args, problems, device, sets, steps):
-    """The same metric through the public torch API from host buffers: every
-    step copies the step's activations (all calls' x, one pinned host buffer)
-    to the device, runs the layer once per problem into its slice of one
-    device output buffer, and reads all outputs back into pinned host memory."""
+    """The same metric through the public torch API from host buffers. Every
+    step copies each call's activations from pinned host memory to the
+    device, runs the layer once per problem (`linear_forward`, eager) into
+    its slice of one device output buffer, and reads every output back into
+    pinned host memory. The copies run on two copy streams and overlap the
+    computation, call by call: call j's input copy, its forward and its
+    output copy are ordered by events, and so are the next step's uses of
+    the same device buffers (its input copy waits for the forward that read
+    the buffer, its forward for the output copy that read y)."""
     from bit_weight_quantized_awq_gb300 import Path, linear_forward
     items = sets[0]
     x_sizes = [it["x"].numel() for it in items]
@@ -449,32 +454,59 @@ def run_e2e(args, problems, device, sets, steps):
     yh = torch.empty(sum(y_sizes), dtype=torch.float16).pin_memory()
     xd = torch.empty(sum(x_sizes), dtype=torch.float16, device=device)
     yd = torch.empty(sum(y_sizes), dtype=torch.float16, device=device)
-    xs, ys, o = [], [], 0
+    xs, ys, xhs, yhs, o = [], [], [], [], 0
     for it, n in zip(items, x_sizes):
         xh[o:o + n].copy_(it["x"].reshape(-1).cpu())
         xs.append(xd[o:o + n].view(it["x"].shape))
+        xhs.append(xh[o:o + n].view(it["x"].shape))
         o += n
     o = 0
     for it, n in zip(items, y_sizes):
         ys.append(yd[o:o + n].view(it["y"].shape))
+        yhs.append(yh[o:o + n].view(it["y"].shape))
         o += n
     path = Path[args.path.upper()]
     h2d = xh.numel() * 2
     d2h = yh.numel() * 2
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    s_c = torch.cuda.current_stream(device)
+    n = len(items)
+    ev_in = [torch.cuda.Event() for _ in range(n)]     # x_j on the device
+    ev_c = [torch.cuda.Event() for _ in range(n)]      # forward j done (x_j read, y_j written)
+    ev_out = [torch.cuda.Event() for _ in range(n)]    # y_j read back
+    started = [False]
 
     def one_step():
-        xd.copy_(xh, non_blocking=True)
         for j, it in enumerate(items):
+            with torch.cuda.stream(s_in):
+                if started[0]:
+                    s_in.wait_event(ev_c[j])
+                xs[j].copy_(xhs[j], non_blocking=True)
+                ev_in[j].record(s_in)
+            s_c.wait_event(ev_in[j])
+            if started[0]:
+                s_c.wait_event(ev_out[j])
             linear_forward(xs[j], it["qweight"], it["qzeros"], it["scales"], it["bias"],
                            it["shape"][3], path=path, out=ys[j])
-        yh.copy_(yd, non_blocking=True)
+            ev_c[j].record(s_c)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_c[j])
+                yhs[j].copy_(ys[j], non_blocking=True)
+                ev_out[j].record(s_out)
+        started[0] = True
+
+    def drain():
+        for st in (s_in, s_c, s_out):
+            st.synchronize()
 
     for _ in range(max(3, args.warmup // 10)):
         one_step()
+    drain()
     barrier(device)
     t0 = time.perf_counter()
     for _ in range(steps):
         one_step()
+    drain()
     barrier(device)
     return time.perf_counter() - t0, h2d, d2h
 
@@ -1014,8 +1046,9 @@ def main():
         "per_problem": per,
         "e2e": {"value": e2e_units / e2e_el / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "api": "bit_weight_quantized_awq_gb300.linear_forward, eager; per step one pinned "
-                       "host-to-device copy of all x and one device-to-host copy of all y"},
+                "api": "bit_weight_quantized_awq_gb300.linear_forward, eager; per step and call a "
+                       "host-to-device copy of x from pinned memory and a device-to-host copy of y into "
+                       "pinned memory, on two copy streams overlapping the computation"},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
