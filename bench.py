@@ -440,29 +440,34 @@ def run_e2e(args, problems, device, sets, steps):
     """The same metric through the public torch API from host buffers. Every
     step copies each call's activations from pinned host memory to the
     device, runs the layer once per problem (`linear_forward`, eager) into
-    its slice of one device output buffer, and reads every output back into
+    its slice of a device output buffer, and reads every output back into
     pinned host memory. The copies run on two copy streams and overlap the
-    computation, call by call: call j's input copy, its forward and its
-    output copy are ordered by events, and so are the next step's uses of
-    the same device buffers (its input copy waits for the forward that read
-    the buffer, its forward for the output copy that read y)."""
+    computation, call by call. The device buffers are double-buffered by
+    step parity, so a step's input copies wait only for the forwards of two
+    steps back that read the same buffer, not for the step before. Events
+    order the rest: call j's input copy, its forward and its output copy;
+    a forward also waits for the output copy of two steps back that read
+    its y buffer."""
     from bit_weight_quantized_awq_gb300 import Path, linear_forward
     items = sets[0]
     x_sizes = [it["x"].numel() for it in items]
     y_sizes = [it["y"].numel() for it in items]
     xh = torch.empty(sum(x_sizes), dtype=torch.float16).pin_memory()
     yh = torch.empty(sum(y_sizes), dtype=torch.float16).pin_memory()
-    xd = torch.empty(sum(x_sizes), dtype=torch.float16, device=device)
-    yd = torch.empty(sum(y_sizes), dtype=torch.float16, device=device)
-    xs, ys, xhs, yhs, o = [], [], [], [], 0
+    xd = [torch.empty(sum(x_sizes), dtype=torch.float16, device=device) for _ in range(2)]
+    yd = [torch.empty(sum(y_sizes), dtype=torch.float16, device=device) for _ in range(2)]
+    xs, ys, xhs, yhs = [[], []], [[], []], [], []
+    o = 0
     for it, n in zip(items, x_sizes):
         xh[o:o + n].copy_(it["x"].reshape(-1).cpu())
-        xs.append(xd[o:o + n].view(it["x"].shape))
+        for b in range(2):
+            xs[b].append(xd[b][o:o + n].view(it["x"].shape))
         xhs.append(xh[o:o + n].view(it["x"].shape))
         o += n
     o = 0
     for it, n in zip(items, y_sizes):
-        ys.append(yd[o:o + n].view(it["y"].shape))
+        for b in range(2):
+            ys[b].append(yd[b][o:o + n].view(it["y"].shape))
         yhs.append(yh[o:o + n].view(it["y"].shape))
         o += n
     path = Path[args.path.upper()]
@@ -471,29 +476,32 @@ def run_e2e(args, problems, device, sets, steps):
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     s_c = torch.cuda.current_stream(device)
     n = len(items)
-    ev_in = [torch.cuda.Event() for _ in range(n)]     # x_j on the device
-    ev_c = [torch.cuda.Event() for _ in range(n)]      # forward j done (x_j read, y_j written)
-    ev_out = [torch.cuda.Event() for _ in range(n)]    # y_j read back
-    started = [False]
+    ev_in = [[torch.cuda.Event() for _ in range(n)] for _ in range(2)]     # x_j on the device
+    ev_c = [[torch.cuda.Event() for _ in range(n)] for _ in range(2)]      # forward j done
+    ev_out = [[torch.cuda.Event() for _ in range(n)] for _ in range(2)]    # y_j read back
+    used = [False, False]
+    step_no = [0]
 
     def one_step():
+        b = step_no[0] & 1
         for j, it in enumerate(items):
             with torch.cuda.stream(s_in):
-                if started[0]:
-                    s_in.wait_event(ev_c[j])
-                xs[j].copy_(xhs[j], non_blocking=True)
-                ev_in[j].record(s_in)
-            s_c.wait_event(ev_in[j])
-            if started[0]:
-                s_c.wait_event(ev_out[j])
-            linear_forward(xs[j], it["qweight"], it["qzeros"], it["scales"], it["bias"],
-                           it["shape"][3], path=path, out=ys[j])
-            ev_c[j].record(s_c)
+                if used[b]:
+                    s_in.wait_event(ev_c[b][j])
+                xs[b][j].copy_(xhs[j], non_blocking=True)
+                ev_in[b][j].record(s_in)
+            s_c.wait_event(ev_in[b][j])
+            if used[b]:
+                s_c.wait_event(ev_out[b][j])
+            linear_forward(xs[b][j], it["qweight"], it["qzeros"], it["scales"], it["bias"],
+                           it["shape"][3], path=path, out=ys[b][j])
+            ev_c[b][j].record(s_c)
             with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_c[j])
-                yhs[j].copy_(ys[j], non_blocking=True)
-                ev_out[j].record(s_out)
-        started[0] = True
+                s_out.wait_event(ev_c[b][j])
+                yhs[j].copy_(ys[b][j], non_blocking=True)
+                ev_out[b][j].record(s_out)
+        used[b] = True
+        step_no[0] += 1
 
     def drain():
         for st in (s_in, s_c, s_out):
@@ -1048,7 +1056,8 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "api": "bit_weight_quantized_awq_gb300.linear_forward, eager; per step and call a "
                        "host-to-device copy of x from pinned memory and a device-to-host copy of y into "
-                       "pinned memory, on two copy streams overlapping the computation"},
+                       "pinned memory, on two copy streams overlapping the computation (device x and y "
+                       "double-buffered by step parity)"},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
