@@ -74,10 +74,10 @@ NCU_TRAFFIC = {
         "summary": "profiles/decode_kernel_decode-7b.md (30 decode launches of one pass of the full workload)",
     },
     ("full", "tcgen05"): {
-        "bytes_per_launch": 811090043,
+        "bytes_per_launch": 818316780,
         "sources": {
             "bit_weight_quantized_awq_gb300/csrc/awq_prefill.cu":
-                "0bd7f9e9268e4daf754f9336d6cb2a15d7fa2f73639bd85e741278b4a5044ed4",
+                "9c9880b53370af89070a66291d03fa476f3a3d040e6344662ffc0ce36e998030",
             "bit_weight_quantized_awq_gb300/csrc/awq_tcgen05.cuh":
                 "7583bdc482c3f999df48aafe74db217e2c2055ec6f41779622d85db462730d4a",
             "bit_weight_quantized_awq_gb300/csrc/awq_dequant.cu":

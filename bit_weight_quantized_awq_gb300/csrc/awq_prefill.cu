@@ -484,6 +484,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     }
                     const uint32_t st = ptx::smem_addr(smem + s * C::kStageBytes);
                     const uint32_t bb = ptx::smem_addr(smem + C::kBSlotOff + b * kBBytes) + b_in;
+                    // all of this thread's packed words of the stage are
+                    // requested before any is converted, so their latencies
+                    // overlap instead of adding up word by word
+                    uint32_t v[BK / 8];
+#pragma unroll
+                    for (int i = 0; i < BK / 8; ++i)
+                        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v[i]) : "r"(st + p_in + i * 1024));
                     uint32_t S[4], Z[4];
                     int r = 0, rem = 0;
                     if (kWhole) {
@@ -506,10 +513,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                                 load_group(st + s_in + r * (BN * 2), st + z_in + r * (BN / 8 * 4), S, Z);
                             }
                         }
-                        uint32_t v;
-                        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(st + p_in + i * 1024));
                         uint32_t h[4];
-                        dequant_word(v, S, Z, h);
+                        dequant_word(v[i], S, Z, h);
                         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                                      ::"r"(bb + i * kBKGroupStride), "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
                                      : "memory");
