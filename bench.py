@@ -74,10 +74,10 @@ NCU_TRAFFIC = {
         "summary": "profiles/decode_kernel_decode-7b.md (30 decode launches of one pass of the full workload)",
     },
     ("full", "tcgen05"): {
-        "bytes_per_launch": 818316780,
+        "bytes_per_launch": 814108508,
         "sources": {
             "bit_weight_quantized_awq_gb300/csrc/awq_prefill.cu":
-                "9c9880b53370af89070a66291d03fa476f3a3d040e6344662ffc0ce36e998030",
+                "8d5cb8990dee65c09a5da74d86d8c036efcf871663e02b8f5a691edac2a43ed6",
             "bit_weight_quantized_awq_gb300/csrc/awq_tcgen05.cuh":
                 "7583bdc482c3f999df48aafe74db217e2c2055ec6f41779622d85db462730d4a",
             "bit_weight_quantized_awq_gb300/csrc/awq_dequant.cu":

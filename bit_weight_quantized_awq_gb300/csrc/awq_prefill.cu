@@ -34,10 +34,11 @@
 //               accumulator over. TMEM holds two accumulators: with MH = 1
 //               tiles alternate between them, with MH = 2 a tile's halves use
 //               one each.
-//   warps 10-13 epilogue: tcgen05.ld of the accumulator (each warp its 32
-//               lanes = 32 tokens), + bias, one rounding to fp16, store. The
-//               epilogue of one tile (or half) overlaps the MMAs of the next
-//               tile (or of the other half).
+//   warps 10-17 epilogue: tcgen05.ld of the accumulator (each warp its 32
+//               lanes = 32 tokens, two warps per lane quarter, each half of
+//               the 256 columns), + bias, one rounding to fp16, TMA stores
+//               of 32 x 32 boxes. The epilogue of one tile (or half)
+//               overlaps the MMAs of the next tile (or of the other half).
 //
 // A second build of the same kernel (kDequant = false) loads an already
 // dequantised fp16 W with TMA straight into the B layout; it serves
@@ -71,7 +72,7 @@ constexpr int kMmaK = 16;
 constexpr int kMaxGroupRows = 5;
 
 constexpr int kABytes = BM * BK * 2;            // 16 KB
-constexpr int kEpiWarpBytes = 32 * 128;         // 32 rows x 64 fp16 columns of output
+constexpr int kEpiWarpBytes = 32 * 64;          // 32 rows x 32 fp16 columns of output
 constexpr int kBBytes = BN * BK * 2;            // 32 KB
 constexpr int kPBytes = BK * (BN / 8) * 4;      // 8 KB
 
@@ -97,8 +98,8 @@ struct Cfg {
     static constexpr int kStageBytes = kDequant ? (MH == 1 ? 28 : 44) * 1024 : kATile + kBBytes;
     static constexpr int kBSlots = kDequant ? 2 : 0;
     static constexpr int kBSlotOff = kStages * kStageBytes;
-    static constexpr int kEpiOff = kBSlotOff + kBSlots * kBBytes;   // epilogue staging, 4 KB per warp
-    static constexpr int kBarOff = kEpiOff + 4 * kEpiWarpBytes;
+    static constexpr int kEpiOff = kBSlotOff + kBSlots * kBBytes;   // epilogue staging, 2 KB per warp
+    static constexpr int kBarOff = kEpiOff + 8 * kEpiWarpBytes;
     static constexpr int kSmemBytes = kBarOff + 256 + 1024;
     static_assert(!kDequant || kZOff + kMaxGroupRows * (BN / 8) * 4 <= kStageBytes, "stage layout overflows");
     static_assert(kStageBytes % 1024 == 0 && kBSlotOff % 1024 == 0 && kEpiOff % 1024 == 0,
@@ -118,12 +119,12 @@ constexpr int kBKGroupStride = 1024;     // between 8-row k groups (stride byte 
 // column unperm(q).
 __host__ __device__ constexpr int unperm(int q) { return q < 4 ? 2 * q : 2 * (q - 4) + 1; }
 
-constexpr int kWarps = 14;
+constexpr int kWarps = 18;
 constexpr int kThreads = kWarps * 32;
 constexpr int kDequantWarp0 = 2;
 constexpr int kEpilogueWarp0 = 10;
 constexpr int kDequantThreads = 256;
-constexpr int kEpilogueThreads = 128;
+constexpr int kEpilogueThreads = 256;
 constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
 
 constexpr uint32_t kIdesc = tc::idesc_f16_f32(BM, BN, true);
@@ -531,6 +532,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         // kernel until it completes
         ptx::wait_prerequisites();
         const int q = warp & 3;                 // TMEM lane quarter this warp may read
+        const int ew = warp - kEpilogueWarp0;   // 0..7: two warps per lane quarter
+        const int ch = ew >> 2;                 // accumulator columns 128 ch .. 128 ch + 127
         int acc_it = 0;
         bool ok = true;
         for (int si = 0; si < sg.count && ok; ++si, ++acc_it) {
@@ -550,7 +553,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                                                     (MH * kPartialFloats);
             for (int h = 0; h < MH; ++h) {
                 const int ab = ab0 + h;
-                // the decision to go on is taken together by the four warps,
+                // the decision to go on is taken together by the eight warps,
                 // which meet at a named barrier
                 ok = ptx::named_barrier_and(
                     1, kEpilogueThreads,
@@ -560,60 +563,50 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 const int m = m0 + h * BM + 32 * q + lane;
                 const uint32_t t_acc = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * BN);
                 if (whole && p.y32 == nullptr) {
-                    // ---- whole tile: + bias, one rounding, staged in this
-                    //      warp's buffer (its 32 rows x 64 columns, 128-byte
-                    //      rows with the 128-byte swizzle) and written by a TMA
-                    //      store, which clips rows >= M and columns >= N
-                    const uint32_t stg = ptx::smem_addr(smem + C::kEpiOff + q * kEpiWarpBytes);
+                    // ---- whole tile: + bias, one rounding, staged 32 columns
+                    //      at a time in this warp's 2 KB buffer (32 rows x 64
+                    //      bytes, 64-byte swizzle) and written by a TMA store,
+                    //      which clips rows >= M and columns >= N
+                    const uint32_t stg = ptx::smem_addr(smem + C::kEpiOff + ew * kEpiWarpBytes);
                     const int row0 = m0 + h * BM + 32 * q;
 #pragma unroll 1
-                    for (int c2 = 0; c2 < BN / 64; ++c2) {
-                        const int col = n0 + 64 * c2;
+                    for (int c = 4 * ch; c < 4 * ch + 4; ++c) {
+                        const int col = n0 + 32 * c;
                         if (col >= p.N) break;
                         // the previous store from the buffer has read it
                         if (lane == 0) ptx::bulk_wait_read_all();
                         __syncwarp();
+                        uint32_t raw[32];
+                        tc::ld_32x32b_x32(t_acc + (uint32_t)(32 * c), raw);
+                        tc::ld_wait();
+                        float b[32];
 #pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            uint32_t raw[32];
-                            tc::ld_32x32b_x32(t_acc + (uint32_t)(64 * c2 + 32 * j), raw);
-                            tc::ld_wait();
-                            const int cj = col + 32 * j;
-                            uint32_t hv[16];
-                            if (cj < p.N) {
-                                float b[32];
+                        for (int e = 0; e < 32; ++e) b[e] = 0.f;
+                        if (p.bias) {
+                            __align__(16) __half bh[32];
 #pragma unroll
-                                for (int e = 0; e < 32; ++e) b[e] = 0.f;
-                                if (p.bias) {
-                                    __align__(16) __half bh[32];
+                            for (int v = 0; v < 4; ++v)
+                                reinterpret_cast<uint4 *>(bh)[v] = __ldg(reinterpret_cast<const uint4 *>(p.bias + col) + v);
 #pragma unroll
-                                    for (int v = 0; v < 4; ++v)
-                                        reinterpret_cast<uint4 *>(bh)[v] =
-                                            __ldg(reinterpret_cast<const uint4 *>(p.bias + cj) + v);
-#pragma unroll
-                                    for (int e = 0; e < 32; ++e) b[e] = __half2float(bh[e]);
-                                }
-#pragma unroll
-                                for (int e = 0; e < 16; ++e) {
-                                    const int e0 = 2 * e, e1 = 2 * e + 1;
-                                    const float v0 = __uint_as_float(kDequant ? raw[(e0 & ~7) + unperm(e0 & 7)] : raw[e0]);
-                                    const float v1 = __uint_as_float(kDequant ? raw[(e1 & ~7) + unperm(e1 & 7)] : raw[e1]);
-                                    const __half2 hh = __halves2half2(__float2half_rn(v0 + b[e0]), __float2half_rn(v1 + b[e1]));
-                                    hv[e] = *reinterpret_cast<const uint32_t *>(&hh);
-                                }
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 16; ++e) hv[e] = 0u;
-                            }
-#pragma unroll
-                            for (int v = 0; v < 4; ++v) {
-                                const uint32_t u = (uint32_t)(4 * j + v);
-                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                                             ::"r"(stg + (uint32_t)lane * 128 + ((u ^ (uint32_t)(lane & 7)) << 4)),
-                                               "r"(hv[4 * v]), "r"(hv[4 * v + 1]), "r"(hv[4 * v + 2]), "r"(hv[4 * v + 3])
-                                             : "memory");
-                            }
+                            for (int e = 0; e < 32; ++e) b[e] = __half2float(bh[e]);
                         }
+                        uint32_t hv[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int e0 = 2 * e, e1 = 2 * e + 1;
+                            const float v0 = __uint_as_float(kDequant ? raw[(e0 & ~7) + unperm(e0 & 7)] : raw[e0]);
+                            const float v1 = __uint_as_float(kDequant ? raw[(e1 & ~7) + unperm(e1 & 7)] : raw[e1]);
+                            const __half2 hh = __halves2half2(__float2half_rn(v0 + b[e0]), __float2half_rn(v1 + b[e1]));
+                            hv[e] = *reinterpret_cast<const uint32_t *>(&hh);
+                        }
+                        // row `lane` of the box: 16-byte chunk u at chunk
+                        // u ^ ((row / 2) % 4) of its 64-byte row
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                                         ::"r"(stg + (uint32_t)lane * 64 + (((uint32_t)u ^ (((uint32_t)lane >> 1) & 3u)) << 4)),
+                                           "r"(hv[4 * u]), "r"(hv[4 * u + 1]), "r"(hv[4 * u + 2]), "r"(hv[4 * u + 3])
+                                         : "memory");
                         // the generic-proxy writes are made visible to the TMA
                         ptx::fence_proxy_async_smem();
                         __syncwarp();
@@ -625,7 +618,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 } else if (whole) {
                     // ---- whole tile, row-shard form: y32 += the fp32 sums
 #pragma unroll 1
-                    for (int c = 0; c < BN / 32; ++c) {
+                    for (int c = 4 * ch; c < 4 * ch + 4; ++c) {
                         uint32_t raw[32];
                         tc::ld_32x32b_x32(t_acc + (uint32_t)(32 * c), raw);
                         tc::ld_wait();
@@ -652,7 +645,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     //      grid, sums the pieces of every split tile
                     float *mine = piece + (int64_t)h * kPartialFloats;
 #pragma unroll 1
-                    for (int c = 0; c < BN / 32; ++c) {
+                    for (int c = 4 * ch; c < 4 * ch + 4; ++c) {
                         uint32_t raw[32];
                         tc::ld_32x32b_x32(t_acc + (uint32_t)(32 * c), raw);
                         tc::ld_wait();
@@ -957,8 +950,8 @@ cudaError_t launch(const Problem &pr, const void *w16, cudaStream_t stream, int6
     memset(&ty, 0, sizeof(ty));
     const uint64_t ldy_eff = ldy > 0 ? (uint64_t)ldy : (uint64_t)N;
     if (pr.y32 == nullptr &&
-        !make_map_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.y, N, M, ldy_eff * 2, 64, 32,
-                     CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_map_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr.y, N, M, ldy_eff * 2, 32, 32,
+                     CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
 
     PrefillParams p{};
